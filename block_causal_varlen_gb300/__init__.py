@@ -1,0 +1,217 @@
+"""block_causal_varlen_gb300 -- block-causal (per-document) varlen attention over
+packed sequences, one contiguous context-parallel query chunk at a time, on
+GB300 (sm_103a).
+
+The compute lives in libbd.so (CUDA kernels behind a C ABI, see
+include/bd_attn.h). This module is the thin Python binding with the same
+names: it marshals torch tensors into the ABI's plain pointers and strides.
+
+Tensor layouts (all strided views are accepted; the head dim is contiguous):
+    q, out, dout  bf16 [B, nchunks, L, H, d]        dq fp32, same shape
+    k, v          bf16 [B, Ck, rows, Hkv, d]        dk, dv fp32, same shape
+                  Ck = 1 with all-gathered K/V (row = global row),
+                  Ck = nchunks with needed-only windows (row 0 = kv_start)
+    lse           fp32 [B, nchunks, H, L]
+A whole packed sequence [B, S, H, d] is the view [B, cp, L, H, d].
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from . import _abi
+from ._abi import (BD_KV_GATHER, BD_KV_WINDOW, BDError, bd_chunk_hdr, bd_rowstat, bd_segment_t,  # noqa: F401
+                   bd_tensor, check, load)
+
+__all__ = ["Plan", "bd_segment", "bd_attn_fwd", "bd_attn_bwd", "bd_owner_sum", "bd_check_status",
+           "bd_attn_bwd_workspace", "attn_fwd", "attn_bwd", "BD_KV_GATHER", "BD_KV_WINDOW", "BDError", "load"]
+
+_HDR_FIELDS = ("S", "cp", "rank", "L", "row_offset", "s_valid", "n_pad", "kv_start", "kv_end", "nseg")
+_SEG_FIELDS = ("doc", "q_start", "q_len", "k_start", "k_len", "diag_off")
+
+
+def _i32(arr):
+    a = np.ascontiguousarray(np.asarray(arr, dtype=np.int32))
+    return a, a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def bd_segment(cu_seqlens, S: int, cp: int, rank: int):
+    """Varlen metadata of chunk ``rank``: (header dict, list of segment tuples)."""
+    lib = load()
+    cu, pcu = _i32(cu_seqlens)
+    hdr = bd_chunk_hdr()
+    check(lib.bd_segment(pcu, len(cu) - 1, S, cp, rank, C.byref(hdr), None, 0))
+    segs = (bd_segment_t * max(1, hdr.nseg))()
+    check(lib.bd_segment(pcu, len(cu) - 1, S, cp, rank, C.byref(hdr), segs, hdr.nseg))
+    return ({f: getattr(hdr, f) for f in _HDR_FIELDS},
+            [tuple(getattr(segs[i], f) for f in _SEG_FIELDS) for i in range(hdr.nseg)])
+
+
+class Plan:
+    """Host plan blob (built once per step) and its device copy.
+
+    ``cu_list``: one cu_seqlens list per sequence; ``ranks``: the chunks the
+    plan covers (default: all cp chunks, i.e. the batched single-GPU grid).
+    """
+
+    def __init__(self, cu_list, S, cp, H, Hkv, d, kv_mode=BD_KV_GATHER, ranks=None):
+        lib = load()
+        self.B, self.S, self.cp, self.H, self.Hkv, self.d = len(cu_list), S, cp, H, Hkv, d
+        self.L = S // cp if cp > 0 and S % cp == 0 else None
+        self.kv_mode = kv_mode
+        self.ranks = list(range(cp)) if ranks is None else list(ranks)
+        self.nchunks = len(self.ranks)
+        self.Ck = 1 if kv_mode == BD_KV_GATHER else self.nchunks
+        offs = np.cumsum([0] + [len(c) for c in cu_list]).astype(np.int32)
+        self._cu, pcu = _i32(np.concatenate([np.asarray(c, dtype=np.int32) for c in cu_list]))
+        self._offs, poffs = _i32(offs)
+        self._ranks, pranks = _i32(self.ranks)
+        self._desc = _abi.bd_plan_desc(self.B, S, cp, self.nchunks, pranks, H, Hkv, d, kv_mode, pcu, poffs)
+        nbytes = C.c_size_t()
+        check(lib.bd_plan_bytes(C.byref(self._desc), C.byref(nbytes)))
+        self.nbytes = nbytes.value
+        raw = np.zeros(self.nbytes // 4 + 16, dtype=np.int32)
+        off = (-raw.ctypes.data % 64) // 4
+        self.host = raw[off:off + self.nbytes // 4]
+        self._raw = raw
+        check(lib.bd_plan_build(C.byref(self._desc), C.c_void_p(self.host.ctypes.data), self.nbytes))
+        self.dev = None
+
+    @property
+    def host_ptr(self):
+        return C.c_void_p(self.host.ctypes.data)
+
+    @property
+    def dev_ptr(self):
+        if self.dev is None:
+            raise RuntimeError("plan not uploaded: call .upload(device)")
+        return C.c_void_p(self.dev.data_ptr())
+
+    def upload(self, device="cuda", non_blocking=False):
+        """Copy the plan blob to device memory (once per step)."""
+        src = torch.from_numpy(self.host)
+        if self.dev is None or self.dev.device != torch.device(device):
+            self.dev = torch.empty_like(src, device=device)
+        self.dev.copy_(src, non_blocking=non_blocking)
+        return self
+
+    def useful_pairs(self) -> int:
+        """Unmasked (query, key) pairs per head over the whole plan."""
+        return int(load().bd_plan_useful_pairs(self.host_ptr))
+
+    def chunk(self, item: int):
+        lib = load()
+        hdr = bd_chunk_hdr()
+        check(lib.bd_plan_chunk(self.host_ptr, item, C.byref(hdr), None, 0))
+        segs = (bd_segment_t * max(1, hdr.nseg))()
+        check(lib.bd_plan_chunk(self.host_ptr, item, C.byref(hdr), segs, hdr.nseg))
+        return ({f: getattr(hdr, f) for f in _HDR_FIELDS},
+                [tuple(getattr(segs[i], f) for f in _SEG_FIELDS) for i in range(hdr.nseg)])
+
+    def header(self, field: int) -> int:
+        return int(self.host[field])
+
+    # index of a few header words (see csrc/plan_layout.h)
+    H_NFWD, H_NBWD, H_KV_ROWS, H_FWD_TILES_LO, H_FWD_TILES_HI = 18, 20, 22, 29, 30
+
+    def fwd_tiles(self) -> int:
+        """Key tiles visited by the forward over all work units (each for `slots` heads)."""
+        return (int(self.host[self.H_FWD_TILES_HI]) << 31) | int(self.host[self.H_FWD_TILES_LO])
+
+    def kv_rows(self) -> int:
+        return int(self.host[self.H_KV_ROWS])
+
+
+def _tensor(t: torch.Tensor, name: str) -> bd_tensor:
+    if t.dim() != 5:
+        raise ValueError(f"{name}: expected a 5-D tensor [B, C, rows, heads, d], got {tuple(t.shape)}")
+    if t.stride(4) != 1:
+        raise ValueError(f"{name}: head dim must be contiguous")
+    s = t.stride()
+    return bd_tensor(t.data_ptr(), s[0], s[1], s[2], s[3], t.shape[2], 0)
+
+
+def _rowstat(t: torch.Tensor, name: str) -> bd_rowstat:
+    if t.dim() != 4 or t.stride(3) != 1 or t.dtype != torch.float32:
+        raise ValueError(f"{name}: expected fp32 [B, C, H, L] with L contiguous")
+    s = t.stride()
+    return bd_rowstat(t.data_ptr(), s[0], s[1], s[2])
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name}: must be a CUDA tensor")
+
+
+def bd_attn_fwd(plan: Plan, q, k, v, out, lse, row_offset: int = -1, stream=None):
+    """Forward of every chunk item in ``plan`` (see include/bd_attn.h)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    tq, tk, tv, to = _tensor(q, "q"), _tensor(k, "k"), _tensor(v, "v"), _tensor(out, "out")
+    tl = _rowstat(lse, "lse")
+    check(load().bd_attn_fwd(plan.host_ptr, plan.dev_ptr, C.byref(tq), C.byref(tk), C.byref(tv), row_offset,
+                             C.byref(to), C.byref(tl), _stream(stream)))
+
+
+def bd_attn_bwd_workspace(plan: Plan) -> int:
+    n = C.c_size_t()
+    check(load().bd_attn_bwd_workspace(plan.host_ptr, C.byref(n)))
+    return n.value
+
+
+def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accumulate_dkv=False,
+                stream=None):
+    """Backward of every chunk item in ``plan`` (see include/bd_attn.h)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.float32, n)
+    ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"))]
+    tl = _rowstat(lse, "lse")
+    tdq, tdk, tdv = _tensor(dq, "dq"), _tensor(dk, "dk"), _tensor(dv, "dv")
+    check(load().bd_attn_bwd(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], C.byref(tl), C.byref(tdq),
+                             C.byref(tdk), C.byref(tdv), int(bool(accumulate_dkv)),
+                             C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                             _stream(stream)))
+
+
+def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None):
+    """Add needed-only-window dK/dV partials into owner rows (see include/bd_attn.h)."""
+    ts = [_tensor(x, n) for x, n in ((dk_win, "dk_win"), (dv_win, "dv_win"), (dk, "dk"), (dv, "dv"))]
+    check(load().bd_owner_sum(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], _stream(stream)))
+
+
+def bd_check_status(plan: Plan, reset: bool = True, stream=None):
+    check(load().bd_check_status(plan.dev_ptr, int(reset), _stream(stream)))
+
+
+# ---------------------------------------------------------------- conveniences
+
+def attn_fwd(plan: Plan, q, k, v, stream=None):
+    """Allocate O and LSE and run the forward; returns (out, lse)."""
+    B, Cn, L, H, d = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty(B, Cn, H, L, dtype=torch.float32, device=q.device)
+    bd_attn_fwd(plan, q, k, v, out, lse, stream=stream)
+    return out, lse
+
+
+def attn_bwd(plan: Plan, q, k, v, out, dout, lse, stream=None):
+    """Allocate gradients and run the backward; returns (dq, dk, dv)."""
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(1, bd_attn_bwd_workspace(plan)), dtype=torch.uint8, device=q.device)
+    bd_attn_bwd(plan, q, k, v, out, dout, lse, dq, dk, dv, ws, stream=stream)
+    return dq, dk, dv

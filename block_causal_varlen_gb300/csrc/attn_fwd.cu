@@ -1,0 +1,455 @@
+// Forward of block-causal varlen chunked attention on sm_103a.
+//
+// What it computes (NeMo Automodel page "block-diagonal varlen CP for packed
+// sequences", Summary and Key correctness properties 1-2): for every query row
+// i of a chunk, O_i = softmax_j(scale * q_i . k_j) v_j over the keys j of row
+// i's own document with j <= i, plus LSE_i (natural log, fp32). Rows past the
+// valid length give O = 0 and LSE = -inf.
+//
+// Design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: Q tiles of the two query heads, then a ring of
+//               K/V tiles (128 keys x d) for the work unit's key-tile range
+//               [kt_lo, kt_lo + nt); fully masked tiles are never loaded.
+//   warp 1      allocates TMEM; one thread issues every tcgen05.mma.
+//   warps 4-7   softmax for query head h0   (slot 0, TMEM lanes = rows)
+//   warps 8-11  softmax for query head h0+1 (slot 1), same rows and keys
+// The two slots are two query heads of one GQA group, so each K/V tile in
+// shared memory feeds both; while one slot's softmax runs, the tensor core
+// works on the other slot (S = Q K^T into TMEM, then O += P V with P read
+// straight from TMEM). TMEM columns: S0 [0,128), S1 [128,256), O0 and O1
+// after that; P_s (bf16 pairs) overwrites the first 64 columns of S_s.
+// Online softmax works in the log2 domain and only rescales O when the row
+// maximum grows by more than 2^8 (exact: the final 1/l uses the same stale max).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <math_constants.h>
+
+#include <cstring>
+
+#include "host_util.h"
+#include "plan_layout.h"
+#include "ptx.cuh"
+
+namespace bd {
+using namespace dev;
+
+struct FwdArgs {
+  const int32_t* plan;
+  __nv_bfloat16* o;
+  int64_t o_sb, o_sc, o_sr, o_sh;
+  float* lse;
+  int64_t l_sb, l_sc, l_sh;
+  int32_t L, n_work, slots, Ck;
+  float scale_log2;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
+  static constexpr int kOCol = 256;                   // first O column in TMEM
+  static constexpr int kThreads = 384;
+};
+
+// barrier indices (8 bytes each)
+enum : int {
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 6, B_KVEMPTY = 10, B_SFULL = 14, B_PFULL = 16,
+  B_OFINAL = 18, B_OEMPTY = 20, B_DRAIN = 22, B_COUNT = 23
+};
+
+__device__ __forceinline__ int find_doc_start(const int32_t* segs, int nseg, int row) {
+  int lo = 0, hi = nseg - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const int32_t* g = segs + mid * kSegWords;
+    if (row < g[1]) hi = mid - 1;
+    else if (row >= g[1] + g[2]) lo = mid + 1;
+    else return g[3];
+  }
+  return -1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using Cfg = FwdCfg<D>;
+  constexpr int NST = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + Cfg::kOffQ, sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV;
+  const uint32_t bars = sbase + Cfg::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * B_COUNT + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t* plan = a.plan;
+  const int32_t* work = plan + plan[H_OFF_FWD];
+  const int32_t* items = plan + plan[H_OFF_ITEMS];
+  const int32_t* segs_all = plan + plan[H_OFF_SEGS];
+  const int slots = a.slots;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_KVEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_PFULL + s), 128);
+      mbar_init(bar(B_OFINAL + s), 1);
+      mbar_init(bar(B_OEMPTY + s), 128);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t kv_it = 0, qi = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+        const int32_t* W = work + w * kFwdWords;
+        const int nt = W[F_NT];
+        if (nt == 0) continue;
+        const int32_t* I = items + W[F_ITEM] * kItemWords;
+        const int b = I[I_B], c = I[I_C], kvbuf = I[I_KVBUF], kvbase = I[I_KVBASE];
+        const int g = W[F_H0] / (plan[H_G]);
+        const int kb = kvbuf / a.Ck, kc = kvbuf % a.Ck;
+        if (!(ok = mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag))) break;
+        mbar_expect_tx(bar(B_QFULL), slots * Cfg::kTileBytes);
+        for (int s = 0; s < slots; ++s)
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_5d(sQ + s * Cfg::kTileBytes + hf * 16384, &tm_q, bar(B_QFULL), hf * 64, W[F_H0] + s,
+                        W[F_QTILE] * 128, c, b);
+        ++qi;
+        for (int j = 0; j < nt; ++j, ++kv_it) {
+          const int st = kv_it % NST;
+          if (!(ok = mbar_wait(bar(B_KVEMPTY + st), ((kv_it / NST) & 1) ^ 1, abort_flag))) break;
+          const int row = (W[F_KTLO] + j) * 128 - kvbase;
+          mbar_expect_tx(bar(B_KFULL + st), Cfg::kTileBytes);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_5d(sK + st * Cfg::kTileBytes + hf * 16384, &tm_k, bar(B_KFULL + st), hf * 64, g, row, kc,
+                        kb);
+          mbar_expect_tx(bar(B_VFULL + st), Cfg::kTileBytes);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_5d(sV + st * Cfg::kTileBytes + hf * 16384, &tm_v, bar(B_VFULL + st), hf * 64, g, row, kc,
+                        kb);
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA's shared memory goes away
+        for (int s = 0; s < NST; ++s) {
+          if (kv_it > uint32_t(s)) {
+            const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % NST);
+            mbar_wait_drain(bar(B_KFULL + s), (last / NST) & 1);
+            mbar_wait_drain(bar(B_VFULL + s), (last / NST) & 1);
+          }
+        }
+        if (qi > 0) mbar_wait_drain(bar(B_QFULL), (qi - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int s, int st) {
+        const uint32_t d_t = tmem + s * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(d_t, sdesc_sw128(sQ + s * Cfg::kTileBytes + off, 16, 1024),
+                 sdesc_sw128(sK + st * Cfg::kTileBytes + off, 16, 1024), idS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int s, int st, bool acc) {
+        const uint32_t d_t = tmem + Cfg::kOCol + s * D;
+        const uint32_t p_t = tmem + s * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(d_t, p_t + kk * 8, sdesc_sw128(sV + st * Cfg::kTileBytes + kk * 2048, 16384, 1024), idPV,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      uint32_t kv_it = 0, qi = 0, tcount = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+        const int nt = work[w * kFwdWords + F_NT];
+        if (nt == 0) continue;
+        if (!(ok = mbar_wait(bar(B_QFULL), qi & 1, abort_flag))) break;
+        {
+          const int st0 = kv_it % NST;
+          if (!(ok = mbar_wait(bar(B_KFULL + st0), (kv_it / NST) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_s(0, st0);
+          tc_commit(bar(B_SFULL + 0));
+          if (slots == 2) {
+            issue_s(1, st0);
+            tc_commit(bar(B_SFULL + 1));
+          }
+          if (nt == 1) tc_commit(bar(B_QEMPTY));
+        }
+        for (int j = 1; j <= nt && ok; ++j) {
+          const uint32_t itp = kv_it + j - 1, itn = kv_it + j;
+          const int sp = itp % NST, sn = itn % NST;
+          const uint32_t tp = tcount + j - 1;
+          if (j < nt && !(ok = mbar_wait(bar(B_KFULL + sn), (itn / NST) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(B_VFULL + sp), (itp / NST) & 1, abort_flag))) break;
+          for (int s = 0; s < slots; ++s) {
+            if (!(ok = mbar_wait(bar(B_PFULL + s), tp & 1, abort_flag))) break;
+            if (j == 1 && !(ok = mbar_wait(bar(B_OEMPTY + s), (qi & 1) ^ 1, abort_flag))) break;
+            tc_fence_after();
+            issue_pv(s, sp, j > 1);
+            if (s == slots - 1) tc_commit(bar(B_KVEMPTY + sp));
+            if (j < nt) {
+              issue_s(s, sn);
+              tc_commit(bar(B_SFULL + s));
+              if (s == slots - 1 && j == nt - 1) tc_commit(bar(B_QEMPTY));
+            } else {
+              tc_commit(bar(B_OFINAL + s));
+            }
+          }
+        }
+        kv_it += nt;
+        tcount += nt;
+        ++qi;
+      }
+      if (!ok) {
+        tc_commit(bar(B_DRAIN));
+        mbar_wait_drain(bar(B_DRAIN), 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int s = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + s * 128;
+    const uint32_t tO = tmem + lane_base + Cfg::kOCol + s * D;
+    if (s < slots) {
+      uint32_t tcount = 0, qi = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+        const int32_t* W = work + w * kFwdWords;
+        const int nt = W[F_NT];
+        const int32_t* I = items + W[F_ITEM] * kItemWords;
+        const int b = I[I_B], c = I[I_C];
+        const int h = W[F_H0] + s;
+        const int lrow = W[F_QTILE] * 128 + r;  // row within the chunk
+        const int grow = I[I_ROW0] + lrow;      // global row
+        const bool row_ok = lrow < a.L;
+        int ds = -1;
+        if (row_ok && grow < I[I_SVALID]) ds = find_doc_start(segs_all + I[I_SEG0] * kSegWords, I[I_NSEG], grow);
+        const bool valid = ds >= 0;
+        __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(lrow) * a.o_sr + int64_t(h) * a.o_sh;
+        float* lrow_p = a.lse + b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + lrow;
+        if (nt == 0) {
+          if (row_ok) {
+            uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) reinterpret_cast<uint4*>(orow)[k] = z;
+            *lrow_p = -CUDART_INF_F;
+          }
+          continue;
+        }
+        float m_run = -CUDART_INF_F, l_run = 0.f;
+        for (int j = 0; j < nt; ++j, ++tcount) {
+          if (!(ok = mbar_wait(bar(B_SFULL + s), tcount & 1, abort_flag))) break;
+          tc_fence_after();
+          uint32_t u[4][32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, u[q]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) reg_fence(u[q]);
+          float x[128];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[q][e]);
+          const int c0 = (W[F_KTLO] + j) * 128;
+          const bool full = valid && c0 >= ds && c0 + 127 <= grow;
+          if (!full) {
+#pragma unroll
+            for (int e = 0; e < 128; ++e) {
+              const int col = c0 + e;
+              if (!(valid && col >= ds && col <= grow)) x[e] = -CUDART_INF_F;
+            }
+          }
+          float mx = x[0];
+#pragma unroll
+          for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+          const float m_new = fmaxf(m_run, mx * a.scale_log2);
+          const bool need = m_new > m_run + 8.0f;
+          float factor = 1.f;
+          if (need) {
+            factor = ex2(m_run - m_new);
+            l_run *= factor;
+            m_run = m_new;
+          }
+          if (__any_sync(0xffffffffu, need && j > 0)) {
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t ov[32];
+              tmem_ld32(tO + q * 32, ov);
+              tmem_ld_wait();
+              reg_fence(ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+              tmem_st32(tO + q * 32, ov);
+            }
+          }
+          const float m_eff = (m_run == -CUDART_INF_F) ? 0.f : m_run;
+          float sum = 0.f;
+          uint32_t pk[2][32];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const float p0 = ex2(fmaf(x[2 * e], a.scale_log2, -m_eff));
+            const float p1 = ex2(fmaf(x[2 * e + 1], a.scale_log2, -m_eff));
+            sum += p0 + p1;
+            pk[e >> 5][e & 31] = pack_bf16(p0, p1);
+          }
+          l_run += sum;
+          tmem_st32(tS, pk[0]);
+          tmem_st32(tS + 32, pk[1]);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(B_PFULL + s));
+        }
+        if (!ok) break;
+        if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t ov[32];
+          tmem_ld32(tO + q * 32, ov);
+          tmem_ld_wait();
+          reg_fence(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
+        }
+        if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
+        tc_fence_before();
+        mbar_arrive(bar(B_OEMPTY + s));
+        ++qi;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) {
+    atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
+    atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 1);
+  }
+}
+
+template <int D>
+static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
+                          int grid, cudaStream_t stream) {
+  using Cfg = FwdCfg<D>;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+    attr_done[dev] = true;
+  }
+  bd_fwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bd_fwd_kernel launch");
+  return BD_OK;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
+                               const bd_tensor* v, int32_t row_offset, bd_tensor* out, bd_rowstat* lse,
+                               void* stream) {
+  PlanView pv;
+  int32_t st = view_plan(plan_host, &pv);
+  if (st) return st;
+  if (!plan_dev || reinterpret_cast<uintptr_t>(plan_dev) % 16)
+    return fail(BD_ERR_ARG, "plan_dev NULL or not 16-byte aligned");
+  const int B = pv.hdr(H_B), C = pv.hdr(H_C), L = pv.hdr(H_L), H = pv.hdr(H_H), Hkv = pv.hdr(H_HKV);
+  const int D = pv.hdr(H_D), Ck = pv.hdr(H_CK);
+  if (row_offset >= 0) {
+    if (pv.hdr(H_NITEMS) != B || C != 1)
+      return fail(BD_ERR_PLAN, "row_offset given but the plan holds more than one chunk per sequence");
+    for (int b = 0; b < B; ++b)
+      if (pv.item(b)[I_ROW0] != row_offset)
+        return fail(BD_ERR_PLAN, "row_offset %d differs from the plan's %d", row_offset, pv.item(b)[I_ROW0]);
+  }
+  if ((st = check_tensor(q, "q", 2, B, C, H, true))) return st;
+  if ((st = check_tensor(k, "k", 2, B, Ck, Hkv, true))) return st;
+  if ((st = check_tensor(v, "v", 2, B, Ck, Hkv, true))) return st;
+  if ((st = check_tensor(out, "out", 2, B, C, H, false))) return st;
+  if (!lse || !lse->ptr) return fail(BD_ERR_ARG, "lse: NULL");
+  if (q->rows != L || out->rows != L) return fail(BD_ERR_ARG, "q/out rows must equal L = %d", L);
+  if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
+    return fail(BD_ERR_ARG, "k/v rows %d/%d < %d needed by the plan", k->rows, v->rows, pv.hdr(H_KV_ROWS));
+  if (reinterpret_cast<uintptr_t>(lse->ptr) % 4) return fail(BD_ERR_ALIGN, "lse not 4-byte aligned");
+  CUtensorMap mq, mk, mv;
+  if ((st = make_tmap_bf16(&mq, q, B, C, H, D, "q"))) return st;
+  if ((st = make_tmap_bf16(&mk, k, B, Ck, Hkv, D, "k"))) return st;
+  if ((st = make_tmap_bf16(&mv, v, B, Ck, Hkv, D, "v"))) return st;
+  FwdArgs a;
+  a.plan = static_cast<const int32_t*>(plan_dev);
+  a.o = static_cast<__nv_bfloat16*>(out->ptr);
+  a.o_sb = out->stride_b; a.o_sc = out->stride_c; a.o_sr = out->stride_row; a.o_sh = out->stride_head;
+  a.lse = lse->ptr; a.l_sb = lse->stride_b; a.l_sc = lse->stride_c; a.l_sh = lse->stride_head;
+  a.L = L; a.n_work = pv.hdr(H_NFWD); a.slots = pv.hdr(H_SLOTS); a.Ck = Ck;
+  float scale;
+  const int32_t scale_bits = pv.hdr(H_SCALE_BITS);
+  memcpy(&scale, &scale_bits, 4);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (a.n_work == 0) return ok();
+  int nsm = 0;
+  if ((st = sm_count(&nsm))) return st;
+  const int grid = a.n_work < nsm ? a.n_work : nsm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = D == 128 ? launch_fwd<128>(mq, mk, mv, a, grid, s) : launch_fwd<64>(mq, mk, mv, a, grid, s);
+  if (st) return st;
+  return ok();
+}

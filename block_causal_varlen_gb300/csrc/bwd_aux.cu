@@ -1,0 +1,157 @@
+// Small HBM-bound kernels around the backward main loop, plus status readback.
+//
+//   bd_bwd_pre_kernel   D_i = <dO_i, O_i> in fp32 for every (row, head) of every
+//                       chunk, and zeroes the fp32 dQ accumulator rows.
+//   bd_owner_sum_kernel adds needed-only-window dK/dV partials into the rows'
+//                       owners, chunk by chunk in plan order (deterministic);
+//                       the single-GPU form of the index_add / reduce-scatter
+//                       SUM backward of the needed-only exchange (NeMo
+//                       Automodel page "block-diagonal varlen CP for packed
+//                       sequences", Design overview, exchange.py).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bwd_aux.h"
+#include "host_util.h"
+#include "plan_layout.h"
+
+namespace bd {
+
+// One warp per (item, row, head): lanes cover d/4 columns each.
+template <int D>
+__global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
+  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = int64_t(a.nitems) * a.L * a.H;
+  if (wid >= total) return;
+  const int h = int(wid % a.H);
+  const int l = int((wid / a.H) % a.L);
+  const int item = int(wid / (int64_t(a.H) * a.L));
+  const int b = item / a.C, c = item % a.C;
+  constexpr int PER = D / 32;  // bf16 values per lane
+  const __nv_bfloat16* o = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr + int64_t(h) * a.o_sh + lane * PER;
+  const __nv_bfloat16* g = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr + int64_t(h) * a.g_sh + lane * PER;
+  float acc = 0.f;
+  if (PER == 4) {
+    const uint2 ov = *reinterpret_cast<const uint2*>(o);
+    const uint2 gv = *reinterpret_cast<const uint2*>(g);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+  } else {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o);
+    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g);
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
+    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv));
+    acc = fmaf(x.x, y.x, x.y * y.y);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) a.dstat[(int64_t(item) * a.H + h) * a.L + l] = acc;
+  if (a.dq) {
+    float* dq = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + lane * PER;
+    if (PER == 4) *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+  }
+}
+
+int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
+  const int64_t warps = int64_t(a.nitems) * a.L * a.H;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (blocks == 0) return BD_OK;
+  if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);
+  else bd_bwd_pre_kernel<64><<<unsigned(blocks), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? BD_OK : cuda_fail(e, "bd_bwd_pre_kernel launch");
+}
+
+// One thread per (b, global row, head, 4 columns): sums the chunks' windows in order.
+__global__ void __launch_bounds__(256) bd_owner_sum_kernel(OwnerSumArgs a) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int q4 = a.d / 4;
+  const int64_t total = int64_t(a.B) * a.S * a.Hkv * q4;
+  if (t >= total) return;
+  const int col = int(t % q4) * 4;
+  const int h = int((t / q4) % a.Hkv);
+  const int row = int((t / (int64_t(q4) * a.Hkv)) % a.S);
+  const int b = int(t / (int64_t(q4) * a.Hkv * a.S));
+  const int32_t* items = a.plan + a.plan[H_OFF_ITEMS];
+  float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
+  for (int c = 0; c < a.C; ++c) {
+    const int32_t* I = items + (b * a.C + c) * kItemWords;
+    const int r = row - I[I_KVSTART];
+    if (row < I[I_KVSTART] || row >= I[I_KVEND]) continue;
+    const int64_t off_k = b * a.wk_sb + c * a.wk_sc + int64_t(r) * a.wk_sr + int64_t(h) * a.wk_sh + col;
+    const int64_t off_v = b * a.wv_sb + c * a.wv_sc + int64_t(r) * a.wv_sr + int64_t(h) * a.wv_sh + col;
+    const float4 x = *reinterpret_cast<const float4*>(a.dk_win + off_k);
+    const float4 y = *reinterpret_cast<const float4*>(a.dv_win + off_v);
+    sk.x += x.x; sk.y += x.y; sk.z += x.z; sk.w += x.w;
+    sv.x += y.x; sv.y += y.y; sv.z += y.z; sv.w += y.w;
+  }
+  float4* pk = reinterpret_cast<float4*>(a.dk + b * a.k_sb + int64_t(row) * a.k_sr + int64_t(h) * a.k_sh + col);
+  float4* pv = reinterpret_cast<float4*>(a.dv + b * a.v_sb + int64_t(row) * a.v_sr + int64_t(h) * a.v_sh + col);
+  float4 ok = *pk, ov = *pv;
+  ok.x += sk.x; ok.y += sk.y; ok.z += sk.z; ok.w += sk.w;
+  ov.x += sv.x; ov.y += sv.y; ov.z += sv.z; ov.w += sv.w;
+  *pk = ok;
+  *pv = ov;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
+                                const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream) {
+  PlanView pv;
+  int32_t st = view_plan(plan_host, &pv);
+  if (st) return st;
+  if (!plan_dev) return fail(BD_ERR_ARG, "plan_dev is NULL");
+  if (pv.hdr(H_KVMODE) != BD_KV_WINDOW) return fail(BD_ERR_PLAN, "bd_owner_sum needs a BD_KV_WINDOW plan");
+  const int B = pv.hdr(H_B), C = pv.hdr(H_C), Hkv = pv.hdr(H_HKV), S = pv.hdr(H_S), D = pv.hdr(H_D);
+  if ((st = check_tensor(dk_win, "dk_win", 4, B, C, Hkv, false))) return st;
+  if ((st = check_tensor(dv_win, "dv_win", 4, B, C, Hkv, false))) return st;
+  if ((st = check_tensor(dk, "dk", 4, B, 1, Hkv, false))) return st;
+  if ((st = check_tensor(dv, "dv", 4, B, 1, Hkv, false))) return st;
+  if (dk->rows < S || dv->rows < S) return fail(BD_ERR_ARG, "dk/dv rows must be >= S = %d", S);
+  if (dk_win->rows < pv.hdr(H_KV_ROWS) || dv_win->rows < pv.hdr(H_KV_ROWS))
+    return fail(BD_ERR_ARG, "window rows < %d", pv.hdr(H_KV_ROWS));
+  OwnerSumArgs a;
+  a.plan = static_cast<const int32_t*>(plan_dev);
+  a.dk_win = static_cast<const float*>(dk_win->ptr);
+  a.dv_win = static_cast<const float*>(dv_win->ptr);
+  a.dk = static_cast<float*>(dk->ptr);
+  a.dv = static_cast<float*>(dv->ptr);
+  a.wk_sb = dk_win->stride_b; a.wk_sc = dk_win->stride_c; a.wk_sr = dk_win->stride_row; a.wk_sh = dk_win->stride_head;
+  a.wv_sb = dv_win->stride_b; a.wv_sc = dv_win->stride_c; a.wv_sr = dv_win->stride_row; a.wv_sh = dv_win->stride_head;
+  a.k_sb = dk->stride_b; a.k_sr = dk->stride_row; a.k_sh = dk->stride_head;
+  a.v_sb = dv->stride_b; a.v_sr = dv->stride_row; a.v_sh = dv->stride_head;
+  a.B = B; a.C = C; a.S = S; a.Hkv = Hkv; a.d = D;
+  const int64_t total = int64_t(B) * S * Hkv * (D / 4);
+  bd_owner_sum_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bd_owner_sum_kernel launch");
+  return ok();
+}
+
+extern "C" int32_t bd_check_status(const void* plan_dev, int32_t reset, void* stream) {
+  if (!plan_dev) return fail(BD_ERR_ARG, "plan_dev is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host[2] = {0, 0};
+  const int32_t* p = static_cast<const int32_t*>(plan_dev) + H_STATUS;
+  cudaError_t e = cudaMemcpyAsync(host, p, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "bd_check_status readback");
+  if (reset && (host[0] || host[1])) {
+    e = cudaMemsetAsync(const_cast<int32_t*>(p), 0, sizeof(host), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "bd_check_status reset");
+  }
+  if (host[0] == DEV_TIMEOUT)
+    return fail(BD_ERR_DEVICE_TIMEOUT, "a kernel stopped after a bounded wait timed out (site %d)", host[1]);
+  return ok();
+}

@@ -1,0 +1,33 @@
+// Argument blocks of the backward's auxiliary kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bd {
+
+struct BwdPreArgs {
+  const __nv_bfloat16* o;
+  int64_t o_sb, o_sc, o_sr, o_sh;
+  const __nv_bfloat16* dout;
+  int64_t g_sb, g_sc, g_sr, g_sh;
+  float* dstat;  // [nitems, H, L]
+  float* dq;     // zeroed when non-NULL
+  int64_t q_sb, q_sc, q_sr, q_sh;
+  int32_t nitems, C, L, H;
+};
+
+struct OwnerSumArgs {
+  const int32_t* plan;
+  const float* dk_win;
+  const float* dv_win;
+  float* dk;
+  float* dv;
+  int64_t wk_sb, wk_sc, wk_sr, wk_sh, wv_sb, wv_sc, wv_sr, wv_sh;
+  int64_t k_sb, k_sr, k_sh, v_sb, v_sr, v_sh;
+  int32_t B, C, S, Hkv, d;
+};
+
+int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s);
+
+}  // namespace bd

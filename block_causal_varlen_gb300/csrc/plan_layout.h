@@ -1,0 +1,48 @@
+// Layout of the plan blob that bd_plan_build writes on the host and the
+// kernels read from device memory. All fields are int32; offsets count int32
+// words from the start of the blob.
+#pragma once
+#include <stdint.h>
+
+namespace bd {
+
+constexpr int32_t kPlanMagic = 0x54414442;  // "BDAT"
+constexpr int32_t kPlanVersion = 1;
+constexpr int kTile = 128;                  // rows per query tile and per key tile
+
+// header words
+enum : int {
+  H_MAGIC = 0, H_VERSION, H_WORDS, H_B, H_S, H_CP, H_C, H_L, H_H, H_HKV, H_D,
+  H_KVMODE, H_G, H_NITEMS, H_OFF_ITEMS, H_OFF_SEGS, H_NSEGS, H_OFF_FWD, H_NFWD,
+  H_OFF_BWD, H_NBWD, H_SCALE_BITS, H_KV_ROWS, H_CK, H_SLOTS, H_QTILES,
+  H_USEFUL_LO, H_USEFUL_HI, H_NBUF, H_FWD_TILES_LO, H_FWD_TILES_HI,
+  H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
+  H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
+  kHdrWords = 64
+};
+
+// chunk item words (item = b * C + c)
+enum : int {
+  I_B = 0, I_C, I_RANK, I_ROW0, I_SVALID, I_NPAD, I_KVSTART, I_KVEND, I_SEG0, I_NSEG,
+  I_KVBASE,   // global row held by row 0 of this item's K/V buffer
+  I_KVBUF,    // K/V buffer index: b (GATHER) or b*C + c (WINDOW)
+  I_USEFUL_LO, I_USEFUL_HI, I_RESERVED0, I_RESERVED1,
+  kItemWords = 16
+};
+
+constexpr int kSegWords = 6;  // doc, q_start, q_len, k_start, k_len, diag_off
+
+// forward work unit: one 128-row query tile of one item for `slots` query
+// heads of one K/V head group, visiting key tiles [kt_lo, kt_lo + nt) of
+// the global 128-row grid.
+enum : int { F_ITEM = 0, F_QTILE, F_H0, F_KTLO, F_NT, F_PAD0, F_PAD1, F_PAD2, kFwdWords = 8 };
+
+// backward work unit: one 128-row tile of one K/V buffer (buffer rows
+// [128*kt, 128*kt+128)) for one K/V head, visiting the query tiles of chunk
+// items [item_lo, item_hi) that attend to it.
+enum : int { W_BUF = 0, W_KTILE, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_PAD0, W_PAD1, kBwdWords = 8 };
+
+// device failure codes stored at H_STATUS
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+
+}  // namespace bd

@@ -1,0 +1,220 @@
+/*
+ * bd_attn.h -- C ABI of libbd: block-causal (per-document) varlen attention
+ * over packed multi-document sequences, computed one contiguous
+ * context-parallel query chunk at a time, for sm_103a (GB300).
+ *
+ * What the operation is (NeMo Automodel page "block-diagonal varlen CP for
+ * packed sequences"):
+ *   - documents are packed back to back into one sequence of S rows, their
+ *     boundaries given as cumulative lengths cu_seqlens (Summary);
+ *   - attention is block-causal per document: row i sees row j iff both lie in
+ *     the same document and j <= i; nothing leaks across a document boundary
+ *     (Motivation; Key correctness property 1);
+ *   - S is padded to a multiple of the context-parallel size cp and rank r owns
+ *     the contiguous rows [r*L, (r+1)*L), L = S/cp (Design overview, batch.py);
+ *   - a document straddling the chunk's left edge gives an asymmetric varlen
+ *     segment with more keys than queries, aligned bottom-right (Key
+ *     correctness property 2);
+ *   - K/V reach a chunk either as the whole sequence (fused [K;V] all-gather,
+ *     the default) or needed-only, starting at the first document the chunk
+ *     overlaps (Summary; Design overview, exchange.py);
+ *   - the backward of the all-gather is a reduce-scatter SUM: per-chunk dK/dV
+ *     partials add up at the rows' owner (Design overview, exchange.py);
+ *   - every index a varlen kernel consumes is validated on the host first,
+ *     because a bad offset is an asynchronous illegal memory access, not an
+ *     error (Key correctness property 4).
+ *
+ * Conventions for every call:
+ *   - Return value: BD_OK (0) or a negative bd_status. Nothing is launched
+ *     when a call fails validation. bd_last_error() gives a message for the
+ *     calling thread's last failure.
+ *   - Ownership: the caller allocates every buffer (host plan, device plan,
+ *     tensors, workspace). The library keeps no device allocation of its own.
+ *   - Device calls are asynchronous and ordered on the given cudaStream_t
+ *     (passed as void*; NULL is the legacy default stream). They do no host
+ *     synchronisation.
+ *   - Softmax scale is 1/sqrt(d); LSE is the natural-log log-sum-exp of the
+ *     scaled scores, in fp32. Padding rows (>= cu_seqlens[last]) get O = 0,
+ *     LSE = -inf and zero gradients. GQA maps query head h to key/value head
+ *     h / (H / Hkv).
+ */
+#ifndef BD_ATTN_H
+#define BD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BD_API __attribute__((visibility("default")))
+#else
+#define BD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BD_OK = 0,
+  BD_ERR_ARG = -1,            /* NULL pointer, bad size or bad enum value        */
+  BD_ERR_CU_SEQLENS = -2,     /* cu_seqlens[0] != 0, decreasing, or > S          */
+  BD_ERR_NOT_DIVISIBLE = -3,  /* S % cp != 0: pad S first (bd_padded_len)        */
+  BD_ERR_RANK = -4,           /* rank outside [0, cp)                            */
+  BD_ERR_CAPACITY = -5,       /* output array or workspace too small             */
+  BD_ERR_ALIGN = -6,          /* pointer/stride not 16-byte aligned, d not unit  */
+  BD_ERR_UNSUPPORTED = -7,    /* head dim, head ratio or layout not supported    */
+  BD_ERR_CUDA = -8,           /* a CUDA runtime/driver call failed               */
+  BD_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up waiting and stopped early      */
+  BD_ERR_PLAN = -10           /* plan blob corrupt or built for other shapes     */
+} bd_status;
+
+typedef enum {
+  BD_KV_GATHER = 0, /* K/V buffer row j = global row j (fused all-gather)            */
+  BD_KV_WINDOW = 1  /* K/V buffer of chunk c starts at global row kv_start of c     */
+} bd_kv_mode;
+
+/* One varlen segment of a chunk, in global rows. The segment's queries are
+ * [q_start, q_start+q_len); its keys are [k_start, k_start+k_len) with
+ * k_start = start of document `doc` and k_start+k_len = q_start+q_len. Local
+ * query i (0-based in the segment) sees local key j iff j <= i + diag_off,
+ * diag_off = k_len - q_len (bottom-right alignment). */
+typedef struct {
+  int32_t doc, q_start, q_len, k_start, k_len, diag_off;
+} bd_segment_t;
+
+/* Per-chunk header. row_offset = rank*L. s_valid = cu_seqlens[ndocs]. n_pad =
+ * rows of the chunk at or past s_valid. [kv_start, kv_end) = the needed-only
+ * key window: kv_start = start of the first document the chunk overlaps,
+ * kv_end = min(row_offset + L, s_valid); for an all-padding chunk both equal
+ * min(row_offset, s_valid) and nseg = 0. */
+typedef struct {
+  int32_t S, cp, rank, L, row_offset, s_valid, n_pad, kv_start, kv_end, nseg;
+} bd_chunk_hdr;
+
+/* bd_segment -- varlen metadata of chunk `rank` of `cp` for one packed sequence.
+ *   cu_seqlens  host int32[ndocs+1], cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[ndocs] <= S. Zero-length documents are allowed and
+ *               produce no segment.
+ *   S           padded sequence length, S % cp == 0.
+ *   hdr         host output header (required).
+ *   segs        host output array of seg_capacity entries, or NULL to only
+ *               count (hdr->nseg is always set).
+ * Errors: BD_ERR_ARG, BD_ERR_CU_SEQLENS, BD_ERR_NOT_DIVISIBLE, BD_ERR_RANK,
+ * BD_ERR_CAPACITY (segs non-NULL and seg_capacity < nseg; hdr still valid).
+ * Pure host function: same inputs, same bytes out. */
+BD_API int32_t bd_segment(const int32_t* cu_seqlens, int32_t ndocs, int32_t S, int32_t cp,
+                   int32_t rank, bd_chunk_hdr* hdr, bd_segment_t* segs,
+                   int32_t seg_capacity);
+
+/* Smallest multiple of cp that is >= s (the padding step of batch.py). */
+BD_API int32_t bd_padded_len(int32_t s, int32_t cp);
+
+/* Description of a step's work: B packed sequences of padded length S, each cut
+ * into cp chunks of L = S/cp rows, of which the plan covers `nchunks` (chunk c
+ * of the plan is rank ranks[c]; ranks == NULL means ranks 0..nchunks-1). One
+ * plan serves one chunk (a per-rank call) or all chunks of all sequences (the
+ * batched single-GPU grid). */
+typedef struct {
+  int32_t B, S, cp, nchunks;
+  const int32_t* ranks;       /* host int32[nchunks] or NULL                      */
+  int32_t H, Hkv, d;          /* d in {64, 128}; H % Hkv == 0                     */
+  int32_t kv_mode;            /* bd_kv_mode                                       */
+  const int32_t* cu_seqlens;  /* host: all sequences' cu arrays back to back      */
+  const int32_t* cu_offsets;  /* host int32[B+1]: sequence b's array is
+                                 cu_seqlens[cu_offsets[b] .. cu_offsets[b+1])    */
+} bd_plan_desc;
+
+/* Size in bytes of the plan blob for `desc` (validates desc like bd_segment). */
+BD_API int32_t bd_plan_bytes(const bd_plan_desc* desc, size_t* bytes);
+
+/* Build the plan blob into caller-owned host memory `blob` (16-byte aligned,
+ * blob_bytes >= bd_plan_bytes). The caller copies the same bytes once per step
+ * to device memory (16-byte aligned, writable: kernels record a failure
+ * status in it) and passes both copies to the attention calls, which size
+ * their launches from the host copy and read the device copy. */
+BD_API int32_t bd_plan_build(const bd_plan_desc* desc, void* blob, size_t blob_bytes);
+
+/* Read back the header of chunk item `item` (item = b*nchunks + c) and its
+ * segments from a host plan blob. */
+BD_API int32_t bd_plan_chunk(const void* plan_host, int32_t item, bd_chunk_hdr* hdr,
+                      bd_segment_t* segs, int32_t seg_capacity);
+
+/* Useful (unmasked) (query, key) pairs per head over all items of a plan. */
+BD_API int64_t bd_plan_useful_pairs(const void* plan_host);
+
+/* A strided device tensor whose last (head) dimension is contiguous.
+ * Query-like tensors (q, out, dout, dq) are [B, nchunks, L, H, d]; key-like
+ * tensors (k, v, dk, dv) are [B, Ck, rows, Hkv, d] with Ck = 1 for
+ * BD_KV_GATHER (one buffer per sequence, row = global row) and Ck = nchunks
+ * for BD_KV_WINDOW (one window buffer per chunk, row 0 = kv_start of that
+ * chunk). Strides are in elements. `rows` is the extent of the row dimension:
+ * L for query-like tensors, the buffer length for key-like ones (GATHER:
+ * >= s_valid of every sequence; WINDOW: >= kv_end - kv_start of every chunk).
+ * Pointers and the b/c/row/head strides (in bytes) must be 16-byte aligned. */
+typedef struct {
+  void* ptr;
+  int64_t stride_b, stride_c, stride_row, stride_head;
+  int32_t rows;
+  int32_t reserved;
+} bd_tensor;
+
+/* Strided fp32 LSE / softmax-statistics tensor [B, nchunks, H, L], row dim contiguous. */
+typedef struct {
+  float* ptr;
+  int64_t stride_b, stride_c, stride_head;
+} bd_rowstat;
+
+/* bd_attn_fwd -- forward of every chunk item in the plan: for each query row
+ * of each chunk, O = softmax(scale * q K^T restricted to the row's document and
+ * causal past) V and LSE. q, k, v bf16; out bf16 (same layout rules as q);
+ * lse fp32. row_offset: -1 to take every chunk's offset from the plan, or
+ * the expected rank*L of a single-chunk plan (checked; BD_ERR_PLAN if it
+ * differs). Rows of K/V at or past s_valid must hold finite values (they are
+ * multiplied by exact zeros). */
+BD_API int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                    const bd_tensor* k, const bd_tensor* v, int32_t row_offset,
+                    bd_tensor* out, bd_rowstat* lse, void* stream);
+
+/* Workspace bytes bd_attn_bwd needs for this plan (softmax statistics D). */
+BD_API int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes);
+
+/* bd_attn_bwd -- backward of every chunk item in the plan for the loss
+ * sum(out * dout). dq fp32 [B, nchunks, L, H, d] is overwritten. dk, dv fp32
+ * key-like tensors receive each K/V buffer's gradient: in BD_KV_GATHER mode
+ * the contributions of all the plan's chunks of a sequence are summed into
+ * that sequence's buffer (the reduce-scatter SUM done in place); in
+ * BD_KV_WINDOW mode each window buffer receives its own chunk's partial (sum
+ * the partials at their owners with bd_owner_sum). accumulate_dkv = 1 adds
+ * into dk/dv instead of overwriting (summing successive single-chunk calls).
+ * workspace: device memory of bd_attn_bwd_workspace bytes, 256-byte aligned. */
+BD_API int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                    const bd_tensor* k, const bd_tensor* v, const bd_tensor* out,
+                    const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq,
+                    bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* bd_owner_sum -- add the BD_KV_WINDOW partials dk_win/dv_win (key-like fp32,
+ * Ck = nchunks) of every chunk of the plan into owner-row tensors dk/dv
+ * (fp32 [B, 1, S, Hkv, d]): dk[b, kv_start_c + r] += dk_win[b, c, r] for the
+ * window rows r < kv_end_c - kv_start_c. The single-GPU form of the
+ * needed-only exchange's index_add / reduce-scatter SUM backward
+ * (Design overview, exchange.py). Deterministic: chunks are added in order. */
+BD_API int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
+                     const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream);
+
+/* Reads the failure status kernels recorded in the device plan (waits for the
+ * stream). BD_OK, or BD_ERR_DEVICE_TIMEOUT if a kernel gave up waiting.
+ * reset != 0 clears the status afterwards. */
+BD_API int32_t bd_check_status(const void* plan_dev, int32_t reset, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+BD_API const char* bd_last_error(void);
+
+/* Library version, e.g. 100 for 0.1.0. */
+BD_API int32_t bd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_ATTN_H */

@@ -1,0 +1,188 @@
+"""Segmentation: the oracle against a hand-worked fixture and closed forms, then
+the library's bd_segment / plan against the oracle, bit-exact (CPU only)."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "segment_tiny_3docs.txt")
+
+
+def _read_golden():
+    chunks, layout = [], None
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        f = line.split()
+        if f[0] == "layout":
+            S, cp, *cu = map(int, f[1:])
+            layout = (cu, S, cp)
+        elif f[0] == "chunk":
+            rank, row0, sv, npad, ks, ke, nseg, useful = map(int, f[1:])
+            chunks.append(dict(rank=rank, row_offset=row0, s_valid=sv, n_pad=npad, kv_start=ks, kv_end=ke,
+                               nseg=nseg, useful=useful, segs=[]))
+        elif f[0] == "seg":
+            chunks[-1]["segs"].append(tuple(map(int, f[1:])))
+    return layout, chunks
+
+
+def _useful(segs):
+    return sum(ql * (kl - ql) + ql * (ql + 1) // 2 for _, _, ql, _, kl, _ in segs)
+
+
+def test_oracle_segmentation_matches_hand_worked_fixture():
+    (cu, S, cp), chunks = _read_golden()
+    for ch in chunks:
+        got = oracle.segment_chunk(cu, S, cp, ch["rank"])
+        h = got["hdr"]
+        for key in ("row_offset", "s_valid", "n_pad", "kv_start", "kv_end", "nseg"):
+            assert h[key] == ch[key], key
+        assert got["segs"] == ch["segs"]
+        assert _useful(got["segs"]) == ch["useful"]
+    assert sum(c["useful"] for c in chunks) == oracle.useful_pairs(cu, S, cp)
+
+
+def test_oracle_single_document_closed_form():
+    """One document of S rows in cp chunks: chunk r is one segment with queries
+    [rL, (r+1)L), keys [0, (r+1)L) and diagonal offset rL."""
+    S, cp = 1536, 8
+    L = S // cp
+    for r in range(cp):
+        got = oracle.segment_chunk([0, S], S, cp, r)
+        assert got["segs"] == [(0, r * L, L, 0, (r + 1) * L, r * L)]
+        assert got["hdr"]["kv_start"] == 0 and got["hdr"]["kv_end"] == (r + 1) * L
+    assert sum(_useful(oracle.segment_chunk([0, S], S, cp, r)["segs"]) for r in range(cp)) == S * (S + 1) // 2
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_oracle_useful_pairs_closed_form(seed):
+    rng = np.random.default_rng(seed)
+    S, cp = 96, int(rng.choice([1, 2, 3, 4]))
+    cu = workloads.random_layout(rng, S, cp)
+    total = sum(_useful(oracle.segment_chunk(cu, S, cp, r)["segs"]) for r in range(cp))
+    lens = np.diff(cu)
+    assert total == int((lens * (lens + 1) // 2).sum()) == oracle.useful_pairs(cu, S, cp)
+
+
+# ---- the library against the oracle ------------------------------------------------
+
+lib = pytest.importorskip("block_causal_varlen_gb300")
+
+
+def _lib_ok():
+    try:
+        lib.load()
+        return True
+    except RuntimeError:
+        return False
+
+
+pytestmark_lib = pytest.mark.skipif(not _lib_ok(), reason="libbd.so not built")
+
+
+def _compare(cu, S, cp):
+    for r in range(cp):
+        want = oracle.segment_chunk(cu, S, cp, r)
+        hdr, segs = lib.bd_segment(cu, S, cp, r)
+        assert segs == want["segs"], (cu, S, cp, r)
+        for key, val in want["hdr"].items():
+            assert hdr[key] == val, (key, cu, S, cp, r)
+
+
+@pytestmark_lib
+def test_library_matches_fixture_and_oracle():
+    (cu, S, cp), chunks = _read_golden()
+    _compare(cu, S, cp)
+    for ch in chunks:
+        _, segs = lib.bd_segment(cu, S, cp, ch["rank"])
+        assert segs == ch["segs"]
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("seed", range(40))
+def test_library_matches_oracle_random(seed):
+    rng = np.random.default_rng(1000 + seed)
+    cp = int(rng.choice([1, 2, 3, 4, 8]))
+    S = cp * int(rng.integers(1, 40))
+    cu = workloads.random_layout(rng, S, cp, max_docs=int(rng.integers(1, 10)))
+    _compare(cu, S, cp)
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("i", [1, 2, 3, 4, 5])
+def test_library_matches_oracle_on_workloads(i):
+    wl = workloads.config(i)
+    for cu in wl.cu:
+        _compare(cu, wl.S, wl.cp)
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("i", [1, 2, 3, 5])
+def test_plan_items_match_oracle_and_useful_pairs(i):
+    wl = workloads.config(i)
+    for mode in (lib.BD_KV_GATHER, lib.BD_KV_WINDOW):
+        plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode)
+        useful = 0
+        for b, cu in enumerate(wl.cu):
+            for r in range(wl.cp):
+                hdr, segs = plan.chunk(b * wl.cp + r)
+                want = oracle.segment_chunk(cu, wl.S, wl.cp, r)
+                assert segs == want["segs"]
+                assert {k: hdr[k] for k in want["hdr"]} == want["hdr"]
+                useful += _useful(want["segs"])
+        assert plan.useful_pairs() == useful
+        lens = np.concatenate([np.diff(c) for c in wl.cu]) if any(len(c) > 1 for c in wl.cu) else np.zeros(0)
+        assert useful == int((lens * (lens + 1) // 2).sum())
+
+
+@pytestmark_lib
+def test_plan_is_deterministic_bytes():
+    wl = workloads.config(3)
+    a = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=lib.BD_KV_WINDOW)
+    b = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=lib.BD_KV_WINDOW)
+    assert np.array_equal(a.host, b.host)
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("cu,S,cp,rank,status", [
+    ([1, 5], 8, 2, 0, lib.BDError),          # cu[0] != 0
+    ([0, 5, 3], 8, 2, 0, lib.BDError),       # decreasing
+    ([0, 9], 8, 2, 0, lib.BDError),          # beyond S
+    ([0, 5], 9, 2, 0, lib.BDError),          # S not a multiple of cp
+    ([0, 5], 8, 2, 2, lib.BDError),          # rank out of range
+    ([0, 5], 8, 2, -1, lib.BDError),
+    ([0, 5], 8, 0, 0, lib.BDError),          # cp = 0
+])
+def test_library_rejects_bad_metadata(cu, S, cp, rank, status):
+    with pytest.raises(status) as e:
+        lib.bd_segment(cu, S, cp, rank)
+    assert e.value.status in (lib._abi.BD_ERR_CU_SEQLENS, lib._abi.BD_ERR_NOT_DIVISIBLE, lib._abi.BD_ERR_RANK,
+                              lib._abi.BD_ERR_ARG)
+
+
+@pytestmark_lib
+def test_library_reports_capacity():
+    import ctypes as C
+    L = lib.load()
+    cu = (C.c_int32 * 4)(0, 3, 6, 8)
+    hdr = lib.bd_chunk_hdr()
+    segs = (lib.bd_segment_t * 1)()
+    st = L.bd_segment(cu, 3, 8, 1, 0, C.byref(hdr), segs, 1)
+    assert st == lib._abi.BD_ERR_CAPACITY and hdr.nseg == 3
+    assert b"capacity" in L.bd_last_error()
+
+
+@pytestmark_lib
+def test_plan_rejects_bad_desc():
+    with pytest.raises(lib.BDError):
+        lib.Plan([[0, 100]], 100, 3, 4, 4, 64)            # S % cp
+    with pytest.raises(lib.BDError):
+        lib.Plan([[0, 100]], 100, 2, 6, 4, 64)            # H % Hkv
+    with pytest.raises(lib.BDError):
+        lib.Plan([[0, 100]], 100, 2, 4, 4, 96)            # head dim
+    with pytest.raises(lib.BDError):
+        lib.Plan([[0, 100]], 100, 2, 4, 4, 64, ranks=[0, 2])  # rank out of range
