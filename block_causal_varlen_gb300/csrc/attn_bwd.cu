@@ -1,9 +1,452 @@
-// Backward of block-causal varlen chunked attention on sm_103a (main loop: in progress).
+// Backward of block-causal varlen chunked attention on sm_103a.
+//
+// What it computes, for the loss sum(O * dO) (the analytic gradient of the
+// forward of the NeMo Automodel page "block-diagonal varlen CP for packed
+// sequences", with the fused K/V all-gather whose backward is a
+// reduce-scatter SUM, Design overview exchange.py):
+//   P_ij = exp(scale q_i.k_j - LSE_i) on the block-causal mask, else 0
+//   dV_j = sum_i P_ij dO_i          dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i),     D_i = dO_i . O_i
+//   dQ_i = scale sum_j dS_ij k_j    dK_j = scale sum_i dS_ij q_i
+// dK/dV of a K/V head sum over the query heads of its GQA group and, for a
+// shared (all-gathered) K/V buffer, over every chunk of the sequence: that sum
+// is the reduce-scatter SUM done in place.
+//
+// Design (one persistent CTA per SM, 16 warps). A work unit is one 128-row
+// K/V tile of one K/V head; K and V stay in shared memory while the CTA walks
+// every (query tile, query head of the group) step that attends to the tile.
+//   warp 0       TMA producer: K/V once per unit; per step a Q tile (2-stage
+//                ring, with the step's LSE / D / document-start rows) and a dO
+//                tile.
+//   warp 1       TMEM allocation; one thread issues the five tcgen05.mma per
+//                step: S^T = K Q^T, dP^T = V dO^T (TMEM), dV += P^T dO (P^T read
+//                from TMEM), dK += dS^T Q, dQ = dS K (dS^T from shared memory).
+//   warps 4-11   P^T and dS^T for the tile's 128 keys (lane = key row), two
+//                warps per lane quarter, one per 64-query half.
+//   warps 12-15  read dQ out of TMEM into fp32 global reductions; at the end
+//                of a unit write dK (x scale) and dV.
+// TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV, dK after that.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstring>
 
 #include "bwd_aux.h"
 #include "host_util.h"
 #include "plan_layout.h"
+#include "ptx.cuh"
+
+namespace bd {
+using namespace dev;
+
+struct BwdArgs {
+  const int32_t* plan;
+  const float* lse2;
+  const float* dstat;
+  const int32_t* rowds;
+  float* dq;
+  int64_t q_sb, q_sc, q_sr, q_sh;
+  float* dk;
+  int64_t k_sb, k_sc, k_sr, k_sh;
+  float* dv;
+  int64_t v_sb, v_sc, v_sr, v_sh;
+  int32_t L, Lpad, H, G, Ck, n_work, accumulate, dk_rows;
+  float scale, scale_log2;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;          // two stages
+  static constexpr int kOffDO = 4 * kTileBytes;
+  static constexpr int kOffDS = 5 * kTileBytes;         // dS^T, 128 keys x 128 queries bf16
+  static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128], ds[128]
+  static constexpr int kStatBytes = 3 * 512;
+  static constexpr int kOffBar = kOffStat + 2 * kStatBytes;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
+  static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr int kThreads = 512;
+};
+
+enum : int {
+  C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_DOFULL, C_DOEMPTY, C_SFULL, C_DPFULL,
+  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_ACCEMPTY, C_DRAIN, C_COUNT
+};
+
+// Iterates the (item, query tile, head) steps of a backward work unit in the
+// same order for every role.
+struct StepRange {
+  const int32_t* items;
+  int it_lo, it_hi, q_lo, q_hi, L;
+  __device__ bool tiles(int it, int& t0, int& t1, int& r0) const {
+    const int32_t* I = items + it * kItemWords;
+    r0 = I[I_ROW0];
+    const int lo = max(q_lo, r0), hi = min(q_hi, r0 + L);
+    if (lo >= hi) return false;
+    t0 = (lo - r0) >> 7;
+    t1 = (hi - 1 - r0) >> 7;
+    return true;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(512, 1)
+    bd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdArgs a) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV, sQ = sbase + Cfg::kOffQ;
+  const uint32_t sDO = sbase + Cfg::kOffDO, sDS = sbase + Cfg::kOffDS;
+  const uint32_t bars = sbase + Cfg::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * C_COUNT + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t* plan = a.plan;
+  const int32_t* work = plan + plan[H_OFF_BWD];
+  const int32_t* items = plan + plan[H_OFF_ITEMS];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C_COUNT; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(C_PREADY), 256);
+    mbar_init(bar(C_DSREADY), 256);
+    mbar_init(bar(C_DQEMPTY), 128);
+    mbar_init(bar(C_ACCEMPTY), 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      uint32_t u = 0, sc = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+        const int32_t* W = work + w * kBwdWords;
+        if (W[W_NQ] == 0) continue;
+        const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
+        if (!(ok = mbar_wait(bar(C_KVEMPTY), (u & 1) ^ 1, abort_flag))) break;
+        mbar_expect_tx(bar(C_KVFULL), 2 * Cfg::kTileBytes);
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tma_load_5d(sK + hf * 16384, &tm_k, bar(C_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
+          tma_load_5d(sV + hf * 16384, &tm_v, bar(C_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
+        }
+        ++u;
+        const StepRange R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+        for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+          int t0, t1, r0;
+          if (!R.tiles(it, t0, t1, r0)) continue;
+          const int32_t* I = items + it * kItemWords;
+          const int b = I[I_B], c = I[I_C];
+          for (int t = t0; t <= t1 && ok; ++t)
+            for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+              const int h = g * a.G + hh;
+              const int qs = sc & 1;
+              if (!(ok = mbar_wait(bar(C_QEMPTY0 + qs), ((sc >> 1) & 1) ^ 1, abort_flag))) break;
+              mbar_expect_tx(bar(C_QFULL0 + qs), Cfg::kTileBytes + Cfg::kStatBytes);
+              for (int hf = 0; hf < D / 64; ++hf)
+                tma_load_5d(sQ + qs * Cfg::kTileBytes + hf * 16384, &tm_q, bar(C_QFULL0 + qs), hf * 64, h, t * 128,
+                            c, b);
+              const uint32_t st = sbase + Cfg::kOffStat + qs * Cfg::kStatBytes;
+              const int64_t srow = (int64_t(it) * a.H + h) * a.Lpad + t * 128;
+              bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
+              bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
+              bulk_load(st + 1024, a.rowds + int64_t(it) * a.Lpad + t * 128, 512, bar(C_QFULL0 + qs));
+              if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) break;
+              mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
+              for (int hf = 0; hf < D / 64; ++hf)
+                tma_load_5d(sDO + hf * 16384, &tm_do, bar(C_DOFULL), hf * 64, h, t * 128, c, b);
+            }
+        }
+      }
+      if (!ok) {
+        // wait for copies already issued before the shared memory goes away
+        if (u > 0) mbar_wait_drain(bar(C_KVFULL), (u - 1) & 1);
+        for (uint32_t x = (sc > 2 ? sc - 2 : 0); x <= sc; ++x) {
+          mbar_wait_drain(bar(C_QFULL0 + (x & 1)), (x >> 1) & 1);
+          mbar_wait_drain(bar(C_DOFULL), x & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idKM = idesc_bf16(128, D, false, true);   // A K-major, B MN-major
+      constexpr uint32_t idMM = idesc_bf16(128, D, true, true);    // both MN-major
+      auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024); };
+      auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); };
+      uint32_t u = 0, sc = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+        const int32_t* W = work + w * kBwdWords;
+        const int nsteps = W[W_NQ];
+        if (nsteps == 0) continue;
+        if (!(ok = mbar_wait(bar(C_KVFULL), u & 1, abort_flag))) break;
+        for (int s = 0; s < nsteps && ok; ++s, ++sc) {
+          const int qs = sc & 1;
+          const uint32_t sQs = sQ + qs * Cfg::kTileBytes;
+          if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmaj(sK, kk), kmaj(sQs, kk), idSS, kk > 0);
+          tc_commit(bar(C_SFULL));
+          if (!(ok = mbar_wait(bar(C_DOFULL), sc & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDP, kmaj(sV, kk), kmaj(sDO, kk), idSS, kk > 0);
+          tc_commit(bar(C_DPFULL));
+          if (!(ok = mbar_wait(bar(C_PREADY), sc & 1, abort_flag))) break;
+          if (s == 0 && !(ok = mbar_wait(bar(C_ACCEMPTY), (u & 1) ^ 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + Cfg::kColDV, tmem + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), idKM,
+                   (s > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C_DOEMPTY));
+          if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + Cfg::kColDK, kmaj(sDS, kk), mnmaj(sQs, kk), idKM, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + Cfg::kColDP, mnmaj(sDS, kk), mnmaj(sK, kk), idMM, kk > 0);
+          tc_commit(bar(C_QEMPTY0 + qs));
+          tc_commit(bar(C_DQFULL));
+          if (s == nsteps - 1) {
+            tc_commit(bar(C_ACCDONE));
+            tc_commit(bar(C_KVEMPTY));
+          }
+        }
+        ++u;
+      }
+      if (!ok) {
+        tc_commit(bar(C_DRAIN));
+        mbar_wait_drain(bar(C_DRAIN), 0);
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ P^T / dS^T
+    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const int jl = quarter * 32 + lane;  // key row within the tile == TMEM lane
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    uint32_t sc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      const int32_t* W = work + w * kBwdWords;
+      if (W[W_NQ] == 0) continue;
+      const int32_t* I0 = items + W[W_ITEM_LO] * kItemWords;
+      const int j = I0[I_KVBASE] + W[W_KTILE] * 128 + jl;  // global key row
+      const StepRange R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+      for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+        int t0, t1, r0;
+        if (!R.tiles(it, t0, t1, r0)) continue;
+        for (int t = t0; t <= t1 && ok; ++t)
+          for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+            const int qs = sc & 1;
+            const int i0 = r0 + t * 128;  // global row of query column 0
+            const float* st_lse = reinterpret_cast<const float*>(smem + Cfg::kOffStat + qs * Cfg::kStatBytes);
+            const float* st_d = st_lse + 128;
+            const int32_t* st_ds = reinterpret_cast<const int32_t*>(st_lse + 256);
+            if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(bar(C_SFULL), sc & 1, abort_flag))) break;
+            tc_fence_after();
+            float p[64];
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + half * 64 + ch * 32, r);
+              tmem_ld_wait();
+              reg_fence(r);
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int i = half * 64 + ch * 32 + e;
+                const bool m = (j >= st_ds[i]) && (j <= i0 + i);
+                const float v = ex2(fmaf(__uint_as_float(r[e]), a.scale_log2, -st_lse[i]));
+                p[ch * 32 + e] = m ? v : 0.f;
+              }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[ch * 32 + 2 * e], p[ch * 32 + 2 * e + 1]);
+              tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C_PREADY));
+            if (!(ok = mbar_wait(bar(C_DPFULL), sc & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t row_addr = sDS + half * 16384 + jl * 128;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + Cfg::kColDP + half * 64 + ch * 32, r);
+              tmem_ld_wait();
+              reg_fence(r);
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int i = half * 64 + ch * 32 + 2 * e;
+                const float d0 = p[ch * 32 + 2 * e] * (__uint_as_float(r[2 * e]) - st_d[i]);
+                const float d1 = p[ch * 32 + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - st_d[i + 1]);
+                pk[e] = pack_bf16(d0, d1);
+              }
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int chunk = ch * 4 + c4;  // 16-byte chunk of the 128-byte row
+                st_shared_v4(row_addr + ((chunk ^ (jl & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2],
+                             pk[4 * c4 + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(C_DSREADY));
+          }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ out, dK/dV epilogue
+    const int quarter = warp & 3;
+    const int rl = quarter * 32 + lane;  // query row (dQ) or key row (dK/dV) == TMEM lane
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    uint32_t u = 0, sc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      const int32_t* W = work + w * kBwdWords;
+      const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
+      const int brow = W[W_KTILE] * 128 + rl;  // buffer row of this lane's key
+      float* dkrow = a.dk + kb * a.k_sb + kc * a.k_sc + int64_t(brow) * a.k_sr + int64_t(g) * a.k_sh;
+      float* dvrow = a.dv + kb * a.v_sb + kc * a.v_sc + int64_t(brow) * a.v_sr + int64_t(g) * a.v_sh;
+      const bool krow_ok = brow < a.dk_rows;
+      if (W[W_NQ] == 0) {
+        if (krow_ok && !a.accumulate) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < D / 4; ++k) {
+            reinterpret_cast<float4*>(dkrow)[k] = z;
+            reinterpret_cast<float4*>(dvrow)[k] = z;
+          }
+        }
+        continue;
+      }
+      const StepRange R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+      for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+        int t0, t1, r0;
+        if (!R.tiles(it, t0, t1, r0)) continue;
+        const int32_t* I = items + it * kItemWords;
+        const int b = I[I_B], c = I[I_C], svalid = I[I_SVALID];
+        for (int t = t0; t <= t1 && ok; ++t)
+          for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+            const int h = g * a.G + hh;
+            const int lrow = t * 128 + rl;
+            const bool qrow_ok = lrow < a.L && r0 + lrow < svalid;
+            float* dqrow = a.dq + b * a.q_sb + c * a.q_sc + int64_t(lrow) * a.q_sr + int64_t(h) * a.q_sh;
+            if (!(ok = mbar_wait(bar(C_DQFULL), sc & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r);
+              tmem_ld_wait();
+              reg_fence(r);
+              if (qrow_ok) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  red_add_v4(dqrow + q * 32 + 4 * e, __uint_as_float(r[4 * e]) * a.scale,
+                             __uint_as_float(r[4 * e + 1]) * a.scale, __uint_as_float(r[4 * e + 2]) * a.scale,
+                             __uint_as_float(r[4 * e + 3]) * a.scale);
+              }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C_DQEMPTY));
+          }
+      }
+      if (!ok) break;
+      if (!(ok = mbar_wait(bar(C_ACCDONE), u & 1, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(tmem + lane_base + Cfg::kColDV + q * 32, rv);
+        tmem_ld32(tmem + lane_base + Cfg::kColDK + q * 32, rk);
+        tmem_ld_wait();
+        reg_fence(rv);
+        reg_fence(rk);
+        if (krow_ok) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 vv = make_float4(__uint_as_float(rv[4 * e]), __uint_as_float(rv[4 * e + 1]),
+                                    __uint_as_float(rv[4 * e + 2]), __uint_as_float(rv[4 * e + 3]));
+            float4 kv = make_float4(__uint_as_float(rk[4 * e]) * a.scale, __uint_as_float(rk[4 * e + 1]) * a.scale,
+                                    __uint_as_float(rk[4 * e + 2]) * a.scale,
+                                    __uint_as_float(rk[4 * e + 3]) * a.scale);
+            float4* pv = reinterpret_cast<float4*>(dvrow + q * 32) + e;
+            float4* pk = reinterpret_cast<float4*>(dkrow + q * 32) + e;
+            if (a.accumulate) {
+              const float4 ov = *pv, ok4 = *pk;
+              vv.x += ov.x; vv.y += ov.y; vv.z += ov.z; vv.w += ov.w;
+              kv.x += ok4.x; kv.y += ok4.y; kv.z += ok4.z; kv.w += ok4.w;
+            }
+            *pv = vv;
+            *pk = kv;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C_ACCEMPTY));
+      ++u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) {
+    atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
+    atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 2);
+  }
+}
+
+template <int D>
+static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const CUtensorMap& mdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+  using Cfg = BwdCfg<D>;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+    attr_done[dev] = true;
+  }
+  bd_bwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bd_bwd_kernel launch");
+  return BD_OK;
+}
+
+}  // namespace bd
 
 using namespace bd;
 
@@ -12,8 +455,7 @@ extern "C" int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes) {
   int32_t st = view_plan(plan_host, &pv);
   if (st) return st;
   if (!bytes) return fail(BD_ERR_ARG, "bytes is NULL");
-  const size_t n = size_t(pv.hdr(H_NITEMS)) * pv.hdr(H_H) * pv.hdr(H_L) * sizeof(float);
-  *bytes = (n + 255) & ~size_t(255);
+  *bytes = bwd_workspace_layout(pv.hdr(H_NITEMS), pv.hdr(H_H), pv.hdr(H_QTILES) * 128).total;
   return ok();
 }
 
@@ -21,10 +463,78 @@ extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, cons
                                const bd_tensor* v, const bd_tensor* out, const bd_tensor* dout,
                                const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
                                int32_t accumulate_dkv, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)plan_dev; (void)q; (void)k; (void)v; (void)out; (void)dout; (void)lse; (void)dq; (void)dk; (void)dv;
-  (void)accumulate_dkv; (void)workspace; (void)workspace_bytes; (void)stream;
   PlanView pv;
   int32_t st = view_plan(plan_host, &pv);
   if (st) return st;
-  return fail(BD_ERR_UNSUPPORTED, "backward not built yet");
+  if (!plan_dev || reinterpret_cast<uintptr_t>(plan_dev) % 16)
+    return fail(BD_ERR_ARG, "plan_dev NULL or not 16-byte aligned");
+  const int B = pv.hdr(H_B), C = pv.hdr(H_C), L = pv.hdr(H_L), H = pv.hdr(H_H), Hkv = pv.hdr(H_HKV);
+  const int D = pv.hdr(H_D), Ck = pv.hdr(H_CK), nitems = pv.hdr(H_NITEMS);
+  const int Lpad = pv.hdr(H_QTILES) * 128;
+  const int kvneed = pv.hdr(H_KVMODE) == BD_KV_GATHER ? pv.hdr(H_S) : pv.hdr(H_KV_ROWS);
+  if ((st = check_tensor(q, "q", 2, B, C, H, true))) return st;
+  if ((st = check_tensor(out, "out", 2, B, C, H, false))) return st;
+  if ((st = check_tensor(dout, "dout", 2, B, C, H, true))) return st;
+  if ((st = check_tensor(k, "k", 2, B, Ck, Hkv, true))) return st;
+  if ((st = check_tensor(v, "v", 2, B, Ck, Hkv, true))) return st;
+  if ((st = check_tensor(dq, "dq", 4, B, C, H, false))) return st;
+  if ((st = check_tensor(dk, "dk", 4, B, Ck, Hkv, false))) return st;
+  if ((st = check_tensor(dv, "dv", 4, B, Ck, Hkv, false))) return st;
+  if (q->rows != L || out->rows != L || dout->rows != L || dq->rows != L)
+    return fail(BD_ERR_ARG, "q/out/dout/dq rows must equal L = %d", L);
+  if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
+    return fail(BD_ERR_ARG, "k/v rows < %d needed by the plan", pv.hdr(H_KV_ROWS));
+  if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
+  if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
+  (void)kvneed;
+  if (!lse || !lse->ptr || reinterpret_cast<uintptr_t>(lse->ptr) % 4) return fail(BD_ERR_ARG, "lse NULL/misaligned");
+  const BwdWorkspace ws = bwd_workspace_layout(nitems, H, Lpad);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(BD_ERR_ALIGN, "workspace NULL or not 256-byte aligned");
+  if (workspace_bytes < ws.total) return fail(BD_ERR_CAPACITY, "workspace needs %zu bytes", ws.total);
+  CUtensorMap mq, mk, mv, mdo;
+  if ((st = make_tmap_bf16(&mq, q, B, C, H, D, "q"))) return st;
+  if ((st = make_tmap_bf16(&mdo, dout, B, C, H, D, "dout"))) return st;
+  if ((st = make_tmap_bf16(&mk, k, B, Ck, Hkv, D, "k"))) return st;
+  if ((st = make_tmap_bf16(&mv, v, B, Ck, Hkv, D, "v"))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* wsb = static_cast<char*>(workspace);
+
+  BwdPreArgs p;
+  p.plan = static_cast<const int32_t*>(plan_dev);
+  p.o = static_cast<const __nv_bfloat16*>(out->ptr);
+  p.o_sb = out->stride_b; p.o_sc = out->stride_c; p.o_sr = out->stride_row; p.o_sh = out->stride_head;
+  p.dout = static_cast<const __nv_bfloat16*>(dout->ptr);
+  p.g_sb = dout->stride_b; p.g_sc = dout->stride_c; p.g_sr = dout->stride_row; p.g_sh = dout->stride_head;
+  p.lse = lse->ptr; p.l_sb = lse->stride_b; p.l_sc = lse->stride_c; p.l_sh = lse->stride_head;
+  p.lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  p.dstat = reinterpret_cast<float*>(wsb + ws.dstat);
+  p.rowds = reinterpret_cast<int32_t*>(wsb + ws.rowds);
+  p.dq = static_cast<float*>(dq->ptr);
+  p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
+  p.nitems = nitems; p.C = C; p.L = L; p.Lpad = Lpad; p.H = H;
+  if ((st = launch_bwd_pre(p, D, s))) return st;
+
+  BwdArgs a;
+  a.plan = p.plan;
+  a.lse2 = p.lse2; a.dstat = p.dstat; a.rowds = p.rowds;
+  a.dq = p.dq; a.q_sb = p.q_sb; a.q_sc = p.q_sc; a.q_sr = p.q_sr; a.q_sh = p.q_sh;
+  a.dk = static_cast<float*>(dk->ptr);
+  a.k_sb = dk->stride_b; a.k_sc = dk->stride_c; a.k_sr = dk->stride_row; a.k_sh = dk->stride_head;
+  a.dv = static_cast<float*>(dv->ptr);
+  a.v_sb = dv->stride_b; a.v_sc = dv->stride_c; a.v_sr = dv->stride_row; a.v_sh = dv->stride_head;
+  a.L = L; a.Lpad = Lpad; a.H = H; a.G = pv.hdr(H_G); a.Ck = Ck; a.n_work = pv.hdr(H_NBWD);
+  a.accumulate = accumulate_dkv ? 1 : 0; a.dk_rows = dk->rows;
+  float scale;
+  const int32_t sb = pv.hdr(H_SCALE_BITS);
+  memcpy(&scale, &sb, 4);
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (a.n_work == 0) return ok();
+  int nsm = 0;
+  if ((st = sm_count(&nsm))) return st;
+  const int grid = a.n_work < nsm ? a.n_work : nsm;
+  st = D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, a, grid, s) : launch_bwd<64>(mq, mk, mv, mdo, a, grid, s);
+  if (st) return st;
+  return ok();
 }

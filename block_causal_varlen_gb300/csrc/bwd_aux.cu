@@ -17,17 +17,54 @@
 
 namespace bd {
 
-// One warp per (item, row, head): lanes cover d/4 columns each.
+BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  BwdWorkspace w;
+  const size_t stat = al(size_t(nitems) * H * Lpad * sizeof(float));
+  w.lse2 = 0;
+  w.dstat = stat;
+  w.rowds = 2 * stat;
+  w.total = 2 * stat + al(size_t(nitems) * Lpad * sizeof(int32_t));
+  return w;
+}
+
+__device__ __forceinline__ int doc_start_of(const int32_t* segs, int nseg, int row) {
+  int lo = 0, hi = nseg - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const int32_t* g = segs + mid * kSegWords;
+    if (row < g[1]) hi = mid - 1;
+    else if (row >= g[1] + g[2]) lo = mid + 1;
+    else return g[3];
+  }
+  return -1;
+}
+
+// One warp per (item, row < Lpad, head): D, log2-domain LSE, the row's document
+// start (head 0 only), and zeroing of the dQ accumulator row.
 template <int D>
 __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t total = int64_t(a.nitems) * a.L * a.H;
+  const int64_t total = int64_t(a.nitems) * a.Lpad * a.H;
   if (wid >= total) return;
   const int h = int(wid % a.H);
-  const int l = int((wid / a.H) % a.L);
-  const int item = int(wid / (int64_t(a.H) * a.L));
+  const int l = int((wid / a.H) % a.Lpad);
+  const int item = int(wid / (int64_t(a.H) * a.Lpad));
   const int b = item / a.C, c = item % a.C;
+  const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+  if (l >= a.L) {
+    if (lane == 0) {
+      a.lse2[sidx] = __int_as_float(0x7f800000);
+      a.dstat[sidx] = 0.f;
+      if (h == 0) a.rowds[int64_t(item) * a.Lpad + l] = 0x7fffffff;
+    }
+    return;
+  }
+  const int32_t* I = a.plan + a.plan[H_OFF_ITEMS] + item * kItemWords;
+  const int grow = I[I_ROW0] + l;
+  int ds = -1;
+  if (grow < I[I_SVALID]) ds = doc_start_of(a.plan + a.plan[H_OFF_SEGS] + I[I_SEG0] * kSegWords, I[I_NSEG], grow);
   constexpr int PER = D / 32;  // bf16 values per lane
   const __nv_bfloat16* o = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr + int64_t(h) * a.o_sh + lane * PER;
   const __nv_bfloat16* g = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr + int64_t(h) * a.g_sh + lane * PER;
@@ -51,16 +88,19 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) a.dstat[(int64_t(item) * a.H + h) * a.L + l] = acc;
-  if (a.dq) {
-    float* dq = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + lane * PER;
-    if (PER == 4) *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+  if (lane == 0) {
+    a.dstat[sidx] = ds >= 0 ? acc : 0.f;
+    const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
+    a.lse2[sidx] = ds >= 0 ? lse * 1.4426950408889634f : __int_as_float(0x7f800000);
+    if (h == 0) a.rowds[int64_t(item) * a.Lpad + l] = ds >= 0 ? ds : 0x7fffffff;
   }
+  float* dq = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + lane * PER;
+  if (PER == 4) *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
+  else *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
 }
 
 int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
-  const int64_t warps = int64_t(a.nitems) * a.L * a.H;
+  const int64_t warps = int64_t(a.nitems) * a.Lpad * a.H;
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks == 0) return BD_OK;
   if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);

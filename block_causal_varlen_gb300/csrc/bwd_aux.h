@@ -7,15 +7,26 @@
 namespace bd {
 
 struct BwdPreArgs {
+  const int32_t* plan;
   const __nv_bfloat16* o;
   int64_t o_sb, o_sc, o_sr, o_sh;
   const __nv_bfloat16* dout;
   int64_t g_sb, g_sc, g_sr, g_sh;
-  float* dstat;  // [nitems, H, L]
-  float* dq;     // zeroed when non-NULL
+  const float* lse;
+  int64_t l_sb, l_sc, l_sh;
+  float* lse2;     // workspace [nitems, H, Lpad]: LSE * log2(e), +inf on invalid rows
+  float* dstat;    // workspace [nitems, H, Lpad]: D = <dO, O>
+  int32_t* rowds;  // workspace [nitems, Lpad]: global start row of the row's document, INT_MAX if invalid
+  float* dq;       // zeroed
   int64_t q_sb, q_sc, q_sr, q_sh;
-  int32_t nitems, C, L, H;
+  int32_t nitems, C, L, Lpad, H;
 };
+
+// Workspace layout of the backward (offsets in bytes, 256-byte aligned).
+struct BwdWorkspace {
+  size_t lse2, dstat, rowds, total;
+};
+BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad);
 
 struct OwnerSumArgs {
   const int32_t* plan;

@@ -253,11 +253,12 @@ int32_t build(const bd_plan_desc* d, Built* out) {
     for (int32_t kt = 0; kt < ntiles; ++kt) {
       const int32_t c0 = kv_base + kt * kTile;
       const int32_t last = std::min(std::min(c0 + kTile, kv_base + rows), svalid) - 1;
-      int32_t nq = 0;
+      int32_t nq = 0, q_lo = c0, q_hi = c0;
       if (last >= c0) {
         // queries attending keys [c0, last]: rows [c0, end of last's document)
         const int32_t* dend = std::upper_bound(cu + 1, cu + nd + 1, last);
         const int32_t q_end = *dend;
+        q_hi = q_end;
         for (int32_t it = it_lo; it < it_hi; ++it) {
           const int32_t* I = &P.items[size_t(it) * kItemWords];
           const int32_t lo = std::max(c0, I[I_ROW0]), hi = std::min(q_end, I[I_ROW0] + L);
@@ -265,7 +266,7 @@ int32_t build(const bd_plan_desc* d, Built* out) {
         }
       }
       for (int32_t g = 0; g < d->Hkv; ++g) {
-        BW w = {{nb, kt, g, it_lo, it_hi, nq * G, 0, 0}};
+        BW w = {{nb, kt, g, it_lo, it_hi, nq * G, q_lo, q_hi}};
         bw.push_back(w);
       }
     }

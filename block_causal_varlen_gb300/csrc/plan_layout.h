@@ -39,8 +39,9 @@ enum : int { F_ITEM = 0, F_QTILE, F_H0, F_KTLO, F_NT, F_PAD0, F_PAD1, F_PAD2, kF
 
 // backward work unit: one 128-row tile of one K/V buffer (buffer rows
 // [128*kt, 128*kt+128)) for one K/V head, visiting the query tiles of chunk
-// items [item_lo, item_hi) that attend to it.
-enum : int { W_BUF = 0, W_KTILE, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_PAD0, W_PAD1, kBwdWords = 8 };
+// items [item_lo, item_hi) that hold global rows in [q_lo, q_hi): the rows
+// that attend to at least one key of the tile (q_lo = q_hi when none).
+enum : int { W_BUF = 0, W_KTILE, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_QLO, W_QHI, kBwdWords = 8 };
 
 // device failure codes stored at H_STATUS
 enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
