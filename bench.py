@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Throughput of block-causal varlen chunked attention (forward + backward).
+
+One step = the whole hot path over one batch of synthetic input: the forward
+of every query chunk of every sequence, then the backward (statistics, main
+kernel) and, for needed-only K/V windows, the owner summation of the dK/dV
+partials. Inputs are resident in HBM when the timed region starts; L2 is
+flushed (256 MiB write) between steps, outside the step's CUDA events.
+
+Headline metric: useful TFLOP/s of forward + backward, where useful FLOPs are
+14 * d * N (N = unmasked (query, key, head) triples; forward 4 d N, backward
+10 d N including the recomputation of Q K^T). Masked pairs are never counted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+With --gpus N > 1 (under torchrun) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful TFLOP/s (fwd, fwd+bwd) and % of GB300 dense BF16 peak, 1 GPU"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                out[k] = float(v) if v is not None else FALLBACK[k]
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def useful_flops(plan, wl):
+    n = plan.useful_pairs() * wl.H
+    return n, 4.0 * wl.d * n, 10.0 * wl.d * n
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_sample(wl, q, k, v, do, chunks, heads):
+    """Time the oracle (fwd + bwd of the given chunks, first `heads` query heads
+    and their K/V head) on the host cores; returns (seconds, useful pairs)."""
+    import torch
+
+    import oracle
+    G = wl.H // wl.Hkv
+    hk = (heads + G - 1) // G
+    pairs = 0
+    t0 = time.perf_counter()
+    for b, c in chunks:
+        hdr = oracle.segment_chunk(wl.cu[b], wl.S, wl.cp, c)
+        h = hdr["hdr"]
+        a, e = h["kv_start"], h["kv_end"]
+        rows = slice(c * wl.L, (c + 1) * wl.L)
+        qs = q[b, rows, :heads]
+        kw, vw = k[b, a:e, :hk], v[b, a:e, :hk]
+        if heads < G:  # keep the grouped head mapping: `heads` query heads on one K/V head
+            kw, vw = k[b, a:e, :1], v[b, a:e, :1]
+        oracle.chunk_fwd(qs, kw, vw, wl.cu[b], wl.S, c * wl.L, kv_base=a)
+        oracle.chunk_bwd(qs, kw, vw, do[b, rows, :heads], wl.cu[b], wl.S, c * wl.L, kv_base=a)
+        pairs += sum(ql * (kl - ql) + ql * (ql + 1) // 2 for _, _, ql, _, kl, _ in hdr["segs"]) * heads
+    del torch
+    return time.perf_counter() - t0, pairs
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores, same metric and workload."""
+    import torch
+
+    import workloads
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    torch.set_num_threads(len(os.sched_getaffinity(0)))
+    wl = workloads.config(args.workload)
+    q, k, v, do = workloads.tensors(wl)
+    chunks_all = [(b, c) for b in range(wl.B) for c in range(wl.cp) if wl.cu[b][-1] > c * wl.L]
+    times, pairs = [], []
+    for s in range(args.warmup + args.steps):
+        t, p = oracle_sample(wl, q, k, v, do, [chunks_all[s % len(chunks_all)]], heads=1)
+        if s >= args.warmup:
+            times.append(t)
+            pairs.append(p)
+    flops = 14.0 * wl.d * sum(pairs)
+    value = flops / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "H": wl.H, "Hkv": wl.Hkv,
+                       "d": wl.d, "kv_mode": wl.kv_mode},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+                             "sample": "each step: one query chunk x one query head (fwd+bwd), chunks in turn"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our path
+
+def run_ours(args):
+    import torch
+
+    import block_causal_varlen_gb300 as bd
+    import workloads
+    from block_causal_varlen_gb300 import build as bdbuild
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bdbuild.build()
+    bd.load()
+
+    wl = workloads.config(args.workload)
+    mode = bd.BD_KV_WINDOW if wl.kv_mode == "window" else bd.BD_KV_GATHER
+    q, k, v, do = workloads.tensors(wl)
+    plan = bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode).upload(dev)
+    n_pairs, f_fwd, f_bwd = useful_flops(plan, wl)
+    f_step = f_fwd + f_bwd
+
+    qd = q.to(dev).view(wl.B, wl.cp, wl.L, wl.H, wl.d)
+    dod = do.to(dev).view_as(qd)
+    if mode == bd.BD_KV_WINDOW:
+        W = plan.kv_rows()
+        kd = torch.zeros(wl.B, wl.cp, W, wl.Hkv, wl.d, dtype=torch.bfloat16, device=dev)
+        vd = torch.zeros_like(kd)
+        for b in range(wl.B):
+            for c in range(wl.cp):
+                hdr, _ = plan.chunk(b * wl.cp + c)
+                a, e = hdr["kv_start"], hdr["kv_end"]
+                kd[b, c, :e - a] = k[b, a:e].to(dev)
+                vd[b, c, :e - a] = v[b, a:e].to(dev)
+    else:
+        kd, vd = k.to(dev).unsqueeze(1), v.to(dev).unsqueeze(1)
+    out = torch.empty_like(qd)
+    lse = torch.empty(wl.B, wl.cp, wl.H, wl.L, dtype=torch.float32, device=dev)
+    dq = torch.empty(qd.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(kd.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    dk_own = torch.zeros(wl.B, 1, wl.S, wl.Hkv, wl.d, dtype=torch.float32, device=dev)
+    dv_own = torch.zeros_like(dk_own)
+    wsp = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 3 + (1 if mode == bd.BD_KV_WINDOW else 0)
+
+    def step(ev):
+        ev[0].record(stream)
+        bd.bd_attn_fwd(plan, qd, kd, vd, out, lse, stream=stream)
+        ev[1].record(stream)
+        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, wsp, stream=stream)
+        ev[2].record(stream)
+        bd.bd_attn_bwd_main(plan, qd, kd, vd, dod, dq, dk, dv, wsp, stream=stream)
+        ev[3].record(stream)
+        if mode == bd.BD_KV_WINDOW:
+            bd.bd_owner_sum(plan, dk, dv, dk_own, dv_own, stream=stream)
+        ev[4].record(stream)
+
+    def prep():
+        flush.zero_()
+        if mode == bd.BD_KV_WINDOW:
+            dk_own.zero_()
+            dv_own.zero_()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for _ in range(args.warmup):
+        prep()
+        step(warm)
+    torch.cuda.synchronize(dev)
+    bd.bd_check_status(plan)
+
+    props = torch.cuda.get_device_properties(dev)
+    clocks = Clocks(f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local))
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for s in range(args.steps):
+        prep()
+        step(evs[s])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    bd.bd_check_status(plan)
+    seg = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]  # ms
+    t_fwd = sum(x[0] for x in seg) / args.steps
+    t_pre = sum(x[1] for x in seg) / args.steps
+    t_main = sum(x[2] for x in seg) / args.steps
+    t_own = sum(x[3] for x in seg) / args.steps
+    t_step = sum(sum(x) for x in seg) / args.steps
+    if ws > 1:
+        tt = torch.tensor([t_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step = float(tt.item())
+    value = ws * f_step / (t_step * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq = qd.cpu().pin_memory()
+        hk = kd.cpu().pin_memory()
+        hv = vd.cpu().pin_memory()
+        hdo = dod.cpu().pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+        hdk = torch.empty(dk_own.shape if mode == bd.BD_KV_WINDOW else dk.shape, dtype=torch.float32).pin_memory()
+        hdv = torch.empty_like(hdk).pin_memory()
+        gk, gv = (dk_own, dv_own) if mode == bd.BD_KV_WINDOW else (dk, dv)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+        e_times = []
+        for s in range(args.warmup + max(3, args.steps // 2)):
+            prep()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            dod.copy_(hdo, non_blocking=True)
+            step(warm)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(gk, non_blocking=True)
+            hdv.copy_(gv, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if s >= args.warmup:
+                e_times.append(e0.elapsed_time(e1))
+        te = sum(e_times) / len(e_times)
+        e2e = {"value": ws * f_step / (te * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": te,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    pk, src = peaks()
+    dominant = "bd_bwd_kernel" if t_main >= t_fwd else "bd_fwd_kernel"
+    dom_ms = t_main if dominant == "bd_bwd_kernel" else t_fwd
+    dom_flops = f_bwd if dominant == "bd_bwd_kernel" else f_fwd
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get(f"{dominant}:{wl.name}")
+        except Exception:
+            traffic = None
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu and ws == 1:
+            import torch as _t
+            _t.set_num_threads(len(os.sched_getaffinity(0)))
+            b0 = 0
+            chunks = [(b0, c) for c in range(wl.cp) if wl.cu[b0][-1] > c * wl.L]
+            secs, pairs = oracle_sample(wl, q, k, v, do, chunks, heads=1)
+            cpu = {"value": 14.0 * wl.d * pairs / secs / 1e12, "unit": "TFLOP/s", "cores": _t.get_num_threads(),
+                   "kind": "oracle", "seconds": secs,
+                   "sample": f"oracle fwd+bwd (fp64) of every chunk of sequence 0, query head 0 only "
+                             f"({pairs} useful pairs); TFLOP/s counts the same useful FLOPs"}
+        result = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "L": wl.L, "H": wl.H,
+                       "Hkv": wl.Hkv, "d": wl.d, "kv_mode": wl.kv_mode, "layout_seed": wl.seed,
+                       "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
+                       "l2": "flushed between steps by a 256 MiB write outside the step events"},
+            "fwd_tflops": f_fwd / (t_fwd * 1e-3) / 1e12,
+            "bwd_tflops": f_bwd / ((t_pre + t_main + t_own) * 1e-3) / 1e12,
+            "fwd_bwd_tflops_12dn": ws * 12.0 * wl.d * n_pairs / (t_step * 1e-3) / 1e12,
+            "frac_of_peak": value / ws / pk["bf16_tflops"],
+            "frac_of_sustained_peak": value / ws / pk["bf16_tflops_sustained"],
+            "peak_source": src,
+            "kernels_ms": {"bd_fwd_kernel": t_fwd, "bd_bwd_pre_kernel": t_pre, "bd_bwd_kernel": t_main,
+                           "bd_owner_sum_kernel": t_own},
+            "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                         "peak_source": f"bf16_tflops ({src})"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3, help="1..5 (default 3: lognormal 16k, GQA, window)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -25,7 +25,8 @@ from . import _abi
 from ._abi import (BD_KV_GATHER, BD_KV_WINDOW, BDError, bd_chunk_hdr, bd_rowstat, bd_segment_t,  # noqa: F401
                    bd_tensor, check, load)
 
-__all__ = ["Plan", "bd_segment", "bd_attn_fwd", "bd_attn_bwd", "bd_owner_sum", "bd_check_status",
+__all__ = ["Plan", "bd_segment", "bd_attn_fwd", "bd_attn_bwd", "bd_attn_bwd_pre", "bd_attn_bwd_main",
+           "bd_owner_sum", "bd_check_status",
            "bd_attn_bwd_workspace", "attn_fwd", "attn_bwd", "BD_KV_GATHER", "BD_KV_WINDOW", "BDError", "load"]
 
 _HDR_FIELDS = ("S", "cp", "rank", "L", "row_offset", "s_valid", "n_pad", "kv_start", "kv_end", "nseg")
@@ -184,6 +185,24 @@ def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accu
                              C.byref(tdk), C.byref(tdv), int(bool(accumulate_dkv)),
                              C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None):
+    """First backward step only: D, log2 LSE, document starts; zeroes dq."""
+    to, tg, tq = _tensor(out, "out"), _tensor(dout, "dout"), _tensor(dq, "dq")
+    tl = _rowstat(lse, "lse")
+    check(load().bd_attn_bwd_pre(plan.host_ptr, plan.dev_ptr, C.byref(to), C.byref(tg), C.byref(tl), C.byref(tq),
+                                 C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)))
+
+
+def bd_attn_bwd_main(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, accumulate_dkv=False, stream=None):
+    """Second backward step only: dq, dk, dv from the workspace bd_attn_bwd_pre filled."""
+    ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
+                                      (dv, "dv"))]
+    check(load().bd_attn_bwd_main(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts],
+                                  int(bool(accumulate_dkv)), C.c_void_p(workspace.data_ptr()),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None):

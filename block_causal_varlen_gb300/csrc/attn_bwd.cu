@@ -114,11 +114,10 @@ __global__ void __launch_bounds__(512, 1)
   const int32_t* items = plan + plan[H_OFF_ITEMS];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C_COUNT; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(C_PREADY), 256);
-    mbar_init(bar(C_DSREADY), 256);
-    mbar_init(bar(C_DQEMPTY), 128);
-    mbar_init(bar(C_ACCEMPTY), 128);
+    for (int i = 0; i < C_COUNT; ++i) {
+      const uint32_t n = (i == C_PREADY || i == C_DSREADY) ? 256u : (i == C_DQEMPTY || i == C_ACCEMPTY) ? 128u : 1u;
+      mbar_init(bar(i), n);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -138,7 +137,7 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      uint32_t u = 0, sc = 0;
+      uint32_t u = 0, sc = 0, q_iss = 0, do_iss = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
         const int32_t* W = work + w * kBwdWords;
@@ -171,20 +170,21 @@ __global__ void __launch_bounds__(512, 1)
               bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
               bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
               bulk_load(st + 1024, a.rowds + int64_t(it) * a.Lpad + t * 128, 512, bar(C_QFULL0 + qs));
+              ++q_iss;
               if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) break;
               mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
               for (int hf = 0; hf < D / 64; ++hf)
                 tma_load_5d(sDO + hf * 16384, &tm_do, bar(C_DOFULL), hf * 64, h, t * 128, c, b);
+              ++do_iss;
             }
         }
       }
       if (!ok) {
         // wait for copies already issued before the shared memory goes away
         if (u > 0) mbar_wait_drain(bar(C_KVFULL), (u - 1) & 1);
-        for (uint32_t x = (sc > 2 ? sc - 2 : 0); x <= sc; ++x) {
+        for (uint32_t x = (q_iss > 2 ? q_iss - 2 : 0); x < q_iss; ++x)
           mbar_wait_drain(bar(C_QFULL0 + (x & 1)), (x >> 1) & 1);
-          mbar_wait_drain(bar(C_DOFULL), x & 1);
-        }
+        if (do_iss > 0) mbar_wait_drain(bar(C_DOFULL), (do_iss - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -459,47 +459,45 @@ extern "C" int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes) {
   return ok();
 }
 
-extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
-                               const bd_tensor* v, const bd_tensor* out, const bd_tensor* dout,
-                               const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
-                               int32_t accumulate_dkv, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+struct BwdCommon {
   PlanView pv;
-  int32_t st = view_plan(plan_host, &pv);
+  int B, C, L, H, Hkv, D, Ck, nitems, Lpad;
+  BwdWorkspace ws;
+};
+
+int32_t bwd_common(const void* plan_host, const void* plan_dev, void* workspace, size_t workspace_bytes,
+                   BwdCommon* c) {
+  int32_t st = view_plan(plan_host, &c->pv);
   if (st) return st;
   if (!plan_dev || reinterpret_cast<uintptr_t>(plan_dev) % 16)
     return fail(BD_ERR_ARG, "plan_dev NULL or not 16-byte aligned");
-  const int B = pv.hdr(H_B), C = pv.hdr(H_C), L = pv.hdr(H_L), H = pv.hdr(H_H), Hkv = pv.hdr(H_HKV);
-  const int D = pv.hdr(H_D), Ck = pv.hdr(H_CK), nitems = pv.hdr(H_NITEMS);
-  const int Lpad = pv.hdr(H_QTILES) * 128;
-  const int kvneed = pv.hdr(H_KVMODE) == BD_KV_GATHER ? pv.hdr(H_S) : pv.hdr(H_KV_ROWS);
-  if ((st = check_tensor(q, "q", 2, B, C, H, true))) return st;
-  if ((st = check_tensor(out, "out", 2, B, C, H, false))) return st;
-  if ((st = check_tensor(dout, "dout", 2, B, C, H, true))) return st;
-  if ((st = check_tensor(k, "k", 2, B, Ck, Hkv, true))) return st;
-  if ((st = check_tensor(v, "v", 2, B, Ck, Hkv, true))) return st;
-  if ((st = check_tensor(dq, "dq", 4, B, C, H, false))) return st;
-  if ((st = check_tensor(dk, "dk", 4, B, Ck, Hkv, false))) return st;
-  if ((st = check_tensor(dv, "dv", 4, B, Ck, Hkv, false))) return st;
-  if (q->rows != L || out->rows != L || dout->rows != L || dq->rows != L)
-    return fail(BD_ERR_ARG, "q/out/dout/dq rows must equal L = %d", L);
-  if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
-    return fail(BD_ERR_ARG, "k/v rows < %d needed by the plan", pv.hdr(H_KV_ROWS));
-  if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
-  if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
-  (void)kvneed;
-  if (!lse || !lse->ptr || reinterpret_cast<uintptr_t>(lse->ptr) % 4) return fail(BD_ERR_ARG, "lse NULL/misaligned");
-  const BwdWorkspace ws = bwd_workspace_layout(nitems, H, Lpad);
+  const PlanView& pv = c->pv;
+  c->B = pv.hdr(H_B); c->C = pv.hdr(H_C); c->L = pv.hdr(H_L); c->H = pv.hdr(H_H); c->Hkv = pv.hdr(H_HKV);
+  c->D = pv.hdr(H_D); c->Ck = pv.hdr(H_CK); c->nitems = pv.hdr(H_NITEMS); c->Lpad = pv.hdr(H_QTILES) * 128;
+  c->ws = bwd_workspace_layout(c->nitems, c->H, c->Lpad);
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(BD_ERR_ALIGN, "workspace NULL or not 256-byte aligned");
-  if (workspace_bytes < ws.total) return fail(BD_ERR_CAPACITY, "workspace needs %zu bytes", ws.total);
-  CUtensorMap mq, mk, mv, mdo;
-  if ((st = make_tmap_bf16(&mq, q, B, C, H, D, "q"))) return st;
-  if ((st = make_tmap_bf16(&mdo, dout, B, C, H, D, "dout"))) return st;
-  if ((st = make_tmap_bf16(&mk, k, B, Ck, Hkv, D, "k"))) return st;
-  if ((st = make_tmap_bf16(&mv, v, B, Ck, Hkv, D, "v"))) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* wsb = static_cast<char*>(workspace);
+  if (workspace_bytes < c->ws.total) return fail(BD_ERR_CAPACITY, "workspace needs %zu bytes", c->ws.total);
+  return BD_OK;
+}
 
+}  // namespace
+
+extern "C" int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, const bd_tensor* out,
+                                   const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  BwdCommon c;
+  int32_t st = bwd_common(plan_host, plan_dev, workspace, workspace_bytes, &c);
+  if (st) return st;
+  if ((st = check_tensor(out, "out", 2, c.B, c.C, c.H, false))) return st;
+  if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, false))) return st;
+  if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, false))) return st;
+  if (out->rows != c.L || dout->rows != c.L || dq->rows != c.L)
+    return fail(BD_ERR_ARG, "out/dout/dq rows must equal L = %d", c.L);
+  if (!lse || !lse->ptr || reinterpret_cast<uintptr_t>(lse->ptr) % 4) return fail(BD_ERR_ARG, "lse NULL/misaligned");
+  char* wsb = static_cast<char*>(workspace);
   BwdPreArgs p;
   p.plan = static_cast<const int32_t*>(plan_dev);
   p.o = static_cast<const __nv_bfloat16*>(out->ptr);
@@ -507,23 +505,55 @@ extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, cons
   p.dout = static_cast<const __nv_bfloat16*>(dout->ptr);
   p.g_sb = dout->stride_b; p.g_sc = dout->stride_c; p.g_sr = dout->stride_row; p.g_sh = dout->stride_head;
   p.lse = lse->ptr; p.l_sb = lse->stride_b; p.l_sc = lse->stride_c; p.l_sh = lse->stride_head;
-  p.lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
-  p.dstat = reinterpret_cast<float*>(wsb + ws.dstat);
-  p.rowds = reinterpret_cast<int32_t*>(wsb + ws.rowds);
+  p.lse2 = reinterpret_cast<float*>(wsb + c.ws.lse2);
+  p.dstat = reinterpret_cast<float*>(wsb + c.ws.dstat);
+  p.rowds = reinterpret_cast<int32_t*>(wsb + c.ws.rowds);
   p.dq = static_cast<float*>(dq->ptr);
   p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
-  p.nitems = nitems; p.C = C; p.L = L; p.Lpad = Lpad; p.H = H;
-  if ((st = launch_bwd_pre(p, D, s))) return st;
+  p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H;
+  if ((st = launch_bwd_pre(p, c.D, static_cast<cudaStream_t>(stream)))) return st;
+  return ok();
+}
 
+extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                                    const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
+                                    bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  BwdCommon c;
+  int32_t st = bwd_common(plan_host, plan_dev, workspace, workspace_bytes, &c);
+  if (st) return st;
+  const PlanView& pv = c.pv;
+  if ((st = check_tensor(q, "q", 2, c.B, c.C, c.H, true))) return st;
+  if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, true))) return st;
+  if ((st = check_tensor(k, "k", 2, c.B, c.Ck, c.Hkv, true))) return st;
+  if ((st = check_tensor(v, "v", 2, c.B, c.Ck, c.Hkv, true))) return st;
+  if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, false))) return st;
+  if ((st = check_tensor(dk, "dk", 4, c.B, c.Ck, c.Hkv, false))) return st;
+  if ((st = check_tensor(dv, "dv", 4, c.B, c.Ck, c.Hkv, false))) return st;
+  if (q->rows != c.L || dout->rows != c.L || dq->rows != c.L)
+    return fail(BD_ERR_ARG, "q/dout/dq rows must equal L = %d", c.L);
+  if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
+    return fail(BD_ERR_ARG, "k/v rows < %d needed by the plan", pv.hdr(H_KV_ROWS));
+  if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
+  if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
+  CUtensorMap mq, mk, mv, mdo;
+  if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q"))) return st;
+  if ((st = make_tmap_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout"))) return st;
+  if ((st = make_tmap_bf16(&mk, k, c.B, c.Ck, c.Hkv, c.D, "k"))) return st;
+  if ((st = make_tmap_bf16(&mv, v, c.B, c.Ck, c.Hkv, c.D, "v"))) return st;
+  char* wsb = static_cast<char*>(workspace);
   BwdArgs a;
-  a.plan = p.plan;
-  a.lse2 = p.lse2; a.dstat = p.dstat; a.rowds = p.rowds;
-  a.dq = p.dq; a.q_sb = p.q_sb; a.q_sc = p.q_sc; a.q_sr = p.q_sr; a.q_sh = p.q_sh;
+  a.plan = static_cast<const int32_t*>(plan_dev);
+  a.lse2 = reinterpret_cast<const float*>(wsb + c.ws.lse2);
+  a.dstat = reinterpret_cast<const float*>(wsb + c.ws.dstat);
+  a.rowds = reinterpret_cast<const int32_t*>(wsb + c.ws.rowds);
+  a.dq = static_cast<float*>(dq->ptr);
+  a.q_sb = dq->stride_b; a.q_sc = dq->stride_c; a.q_sr = dq->stride_row; a.q_sh = dq->stride_head;
   a.dk = static_cast<float*>(dk->ptr);
   a.k_sb = dk->stride_b; a.k_sc = dk->stride_c; a.k_sr = dk->stride_row; a.k_sh = dk->stride_head;
   a.dv = static_cast<float*>(dv->ptr);
   a.v_sb = dv->stride_b; a.v_sc = dv->stride_c; a.v_sr = dv->stride_row; a.v_sh = dv->stride_head;
-  a.L = L; a.Lpad = Lpad; a.H = H; a.G = pv.hdr(H_G); a.Ck = Ck; a.n_work = pv.hdr(H_NBWD);
+  a.L = c.L; a.Lpad = c.Lpad; a.H = c.H; a.G = pv.hdr(H_G); a.Ck = c.Ck; a.n_work = pv.hdr(H_NBWD);
   a.accumulate = accumulate_dkv ? 1 : 0; a.dk_rows = dk->rows;
   float scale;
   const int32_t sb = pv.hdr(H_SCALE_BITS);
@@ -534,7 +564,18 @@ extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, cons
   int nsm = 0;
   if ((st = sm_count(&nsm))) return st;
   const int grid = a.n_work < nsm ? a.n_work : nsm;
-  st = D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, a, grid, s) : launch_bwd<64>(mq, mk, mv, mdo, a, grid, s);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = c.D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, a, grid, s) : launch_bwd<64>(mq, mk, mv, mdo, a, grid, s);
   if (st) return st;
   return ok();
+}
+
+extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
+                               const bd_tensor* v, const bd_tensor* out, const bd_tensor* dout,
+                               const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
+                               int32_t accumulate_dkv, void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t st = bd_attn_bwd_pre(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes, stream);
+  if (st) return st;
+  return bd_attn_bwd_main(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace,
+                          workspace_bytes, stream);
 }

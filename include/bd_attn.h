@@ -193,6 +193,21 @@ BD_API int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd
                     bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* bd_attn_bwd_pre -- the first step of bd_attn_bwd on its own: per row and
+ * head D = <dout, out> (fp32), the LSE in log2 units and each row's document
+ * start, written into `workspace`; zeroes dq. */
+BD_API int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, const bd_tensor* out,
+                        const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* bd_attn_bwd_main -- the second step of bd_attn_bwd on its own: dq (added
+ * into what bd_attn_bwd_pre zeroed), dk and dv from the workspace that
+ * bd_attn_bwd_pre filled for the same plan and tensors. */
+BD_API int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                         const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
+                         bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* bd_owner_sum -- add the BD_KV_WINDOW partials dk_win/dv_win (key-like fp32,
  * Ck = nchunks) of every chunk of the plan into owner-row tensors dk/dv
  * (fp32 [B, 1, S, Hkv, d]): dk[b, kv_start_c + r] += dk_win[b, c, r] for the
