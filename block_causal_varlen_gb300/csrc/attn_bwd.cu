@@ -68,6 +68,9 @@ struct BwdCfg {
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
+  // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
+  static constexpr int kRegsCtl = 56, kRegsCompute = 152, kRegsDq = 136;
+  static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
 };
 
 enum : int {
@@ -129,6 +132,9 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 4) regs_dec<Cfg::kRegsCtl>();
+  else if (warp < 12) regs_inc<Cfg::kRegsCompute>();
+  else regs_inc<Cfg::kRegsDq>();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -438,6 +444,12 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, bd_bwd_kernel<D>);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd)");
+    if (fa.numRegs * Cfg::kThreads < Cfg::kRegsNeeded)
+      return fail(BD_ERR_UNSUPPORTED, "bwd kernel built with %d registers/thread, register split needs %d",
+                  fa.numRegs, (Cfg::kRegsNeeded + Cfg::kThreads - 1) / Cfg::kThreads);
     attr_done[dev] = true;
   }
   bd_bwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, a);

@@ -55,6 +55,10 @@ struct FwdCfg {
   static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr int kOCol = 256;                   // first O column in TMEM
   static constexpr int kThreads = 384;
+  // register split after setmaxnreg: warpgroup 0 (producer, MMA) and the two
+  // softmax warpgroups; the sum must fit in what the launch reserved
+  static constexpr int kRegsCtl = 56, kRegsSoftmax = 200;
+  static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
 };
 
 // barrier indices (8 bytes each)
@@ -124,8 +128,11 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
+  // the softmax warpgroups hold a 128-column score row each: registers move to
+  // them from warpgroup 0 (producer and MMA warps) at the top of each branch
+  if (warp < 4) {
+   regs_dec<Cfg::kRegsCtl>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
@@ -244,7 +251,9 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait_drain(bar(B_DRAIN), 0);
       }
     }
-  } else if (warp >= 4) {
+   }
+  } else {
+    regs_inc<Cfg::kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int s = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -392,6 +401,13 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, bd_fwd_kernel<D>);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
+    // setmaxnreg.inc waits until registers are free: never launch a split that cannot be met
+    if (fa.numRegs * Cfg::kThreads < Cfg::kRegsNeeded)
+      return fail(BD_ERR_UNSUPPORTED, "fwd kernel built with %d registers/thread, register split needs %d",
+                  fa.numRegs, (Cfg::kRegsNeeded + Cfg::kThreads - 1) / Cfg::kThreads);
     attr_done[dev] = true;
   }
   bd_fwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);
