@@ -69,7 +69,7 @@ struct BwdCfg {
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
-  static constexpr int kRegsCtl = 56, kRegsCompute = 152, kRegsDq = 136;
+  static constexpr int kRegsCtl = 72, kRegsCompute = 144, kRegsDq = 136;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
 };
 
@@ -132,11 +132,11 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) regs_dec<Cfg::kRegsCtl>();
-  else if (warp < 12) regs_inc<Cfg::kRegsCompute>();
-  else regs_inc<Cfg::kRegsDq>();
-
-  if (warp == 0) {
+  // registers move from warpgroup 0 (producer, MMA) to the compute warpgroups at
+  // the top of each warpgroup's branch
+  if (warp < 4) {
+   regs_dec<Cfg::kRegsCtl>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(512, 1)
         mbar_wait_drain(bar(C_DRAIN), 0);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+   }
+  } else if (warp < 12) {
+    regs_inc<Cfg::kRegsCompute>();
     // ------------------------------------------------------------ P^T / dS^T
     const int quarter = warp & 3, half = (warp - 4) >> 2;
     const int jl = quarter * 32 + lane;  // key row within the tile == TMEM lane
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(512, 1)
           }
       }
     }
-  } else if (warp >= 12) {
+  } else {
+    regs_inc<Cfg::kRegsDq>();
     // ------------------------------------------------------------ dQ out, dK/dV epilogue
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // query row (dQ) or key row (dK/dV) == TMEM lane

@@ -57,7 +57,7 @@ struct FwdCfg {
   static constexpr int kThreads = 384;
   // register split after setmaxnreg: warpgroup 0 (producer, MMA) and the two
   // softmax warpgroups; the sum must fit in what the launch reserved
-  static constexpr int kRegsCtl = 56, kRegsSoftmax = 200;
+  static constexpr int kRegsCtl = 72, kRegsSoftmax = 216;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
 };
 
