@@ -79,6 +79,11 @@ EXPORTS = {
                                      C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                      C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_int32, C.c_void_p,
                                      C.c_size_t, C.c_void_p]),
+    "bd_attn_bwd_noalloc": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                        C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                        C.POINTER(bd_rowstat), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                        C.POINTER(bd_tensor), C.c_int32, C.c_void_p]),
+    "bd_attn_bwd_noalloc_capacity": (C.c_size_t, []),
     "bd_owner_sum": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                  C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_void_p]),
     "bd_check_status": (C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p]),

@@ -217,6 +217,25 @@ BD_API int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, con
 BD_API int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
                      const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream);
 
+/* bd_attn_bwd_noalloc -- bd_attn_bwd for callers that cannot allocate device
+ * memory (no allocator is available to them, or a memory cap forbids one
+ * more allocation). The paper has no counterpart: it is an addition of this
+ * library. The workspace comes from a fixed 16 MiB array in device global
+ * memory declared by the library (held on every GPU that loads it until exit);
+ * nothing is allocated. Plans needing more workspace than
+ * bd_attn_bwd_noalloc_capacity() return BD_ERR_CAPACITY before any launch.
+ * All calls on a device share the array: calls that may overlap on the GPU
+ * race and must be ordered by the caller. The first call on a device looks up
+ * the array's address; make it before any stream capture. Arguments and
+ * results are those of bd_attn_bwd without the workspace. */
+BD_API int32_t bd_attn_bwd_noalloc(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                            const bd_tensor* k, const bd_tensor* v, const bd_tensor* out,
+                            const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk,
+                            bd_tensor* dv, int32_t accumulate_dkv, void* stream);
+
+/* Bytes of workspace bd_attn_bwd_noalloc can serve. */
+BD_API size_t bd_attn_bwd_noalloc_capacity(void);
+
 /* Reads the failure status kernels recorded in the device plan (waits for the
  * stream). BD_OK, or BD_ERR_DEVICE_TIMEOUT if a kernel gave up waiting.
  * reset != 0 clears the status afterwards. */
