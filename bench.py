@@ -59,7 +59,7 @@ def dist_env():
 class Clocks:
     """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -73,10 +73,15 @@ class Clocks:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        self.window = None
+
+    def mark(self, t0, t1):
+        """Wall-clock bounds of the timed region; only samples inside it count."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -86,23 +91,32 @@ class Clocks:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        import datetime
+        sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if self.window and ts is not None and not (self.window[0] <= ts <= self.window[1]):
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+                power.append(float(f[4]))
             except ValueError:
                 continue
-            for n, val in zip(names, f[5:9]):
+            for n, val in zip(names, f[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "power_w": statistics.median(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
 
 
 def useful_flops(plan, wl):
@@ -244,22 +258,26 @@ def run_ours(args):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     warm = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    props = torch.cuda.get_device_properties(dev)
+    clocks = Clocks(f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local))
+    clocks.start()  # nvidia-smi needs a moment to start: launch it before the warm-up
     for _ in range(args.warmup):
         prep()
         step(warm)
     torch.cuda.synchronize(dev)
     bd.bd_check_status(plan)
 
-    props = torch.cuda.get_device_properties(dev)
-    clocks = Clocks(f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    t_wall0 = time.time()
     for s in range(args.steps):
         prep()
         step(evs[s])
     torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    time.sleep(0.1)
+    clocks.mark(t_wall0, t_wall1)
     clk = clocks.stop()
     if ws > 1:
         torch.distributed.barrier()
@@ -373,7 +391,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=3, help="1..5 (default 3: lognormal 16k, GQA, window)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

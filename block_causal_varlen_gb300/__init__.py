@@ -121,6 +121,12 @@ class Plan:
         """Key tiles visited by the forward over all work units (each for `slots` heads)."""
         return (int(self.host[self.H_FWD_TILES_HI]) << 31) | int(self.host[self.H_FWD_TILES_LO])
 
+    def row_doc_starts(self):
+        """Per chunk item, the global start row of each row's document (int32;
+        2**31 - 1 on padding rows), as the kernels read it from the plan."""
+        off = int(self.host[31])
+        return self.host[off:off + self.B * self.nchunks * self.L].reshape(self.B * self.nchunks, self.L)
+
     def kv_rows(self) -> int:
         return int(self.host[self.H_KV_ROWS])
 

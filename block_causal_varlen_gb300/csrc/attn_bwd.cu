@@ -23,8 +23,9 @@
 //                from TMEM), dK += dS^T Q, dQ = dS K (dS^T from shared memory).
 //   warps 4-11   P^T and dS^T for the tile's 128 keys (lane = key row), two
 //                warps per lane quarter, one per 64-query half.
-//   warps 12-15  read dQ out of TMEM into fp32 global reductions; at the end
-//                of a unit write dK (x scale) and dV.
+//   warps 12-15  read dQ out of TMEM and add it into global memory with TMA
+//                reduce-adds (128 x 32 fp32 boxes staged in shared memory); at
+//                the end of a unit write dK (x scale) and dV.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV, dK after that.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -64,13 +65,16 @@ struct BwdCfg {
   static constexpr int kOffDS = 5 * kTileBytes;         // dS^T, 128 keys x 128 queries bf16
   static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128], ds[128]
   static constexpr int kStatBytes = 3 * 512;
-  static constexpr int kOffBar = kOffStat + 2 * kStatBytes;
+  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;  // dQ staging, 128 rows x 128 bytes
+  static constexpr int kOffBar = kOffStage + 16384;
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
-  static constexpr int kRegsCtl = 72, kRegsCompute = 144, kRegsDq = 136;
+  static constexpr int kRegsCtl = 88, kRegsCompute = 144, kRegsDq = 112;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
+  static constexpr int kRegsLaunch = 128;  // 65536 / 512 threads: what ptxas assigns at launch
+  static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
 };
 
 enum : int {
@@ -98,13 +102,13 @@ template <int D>
 __global__ void __launch_bounds__(512, 1)
     bd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using Cfg = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV, sQ = sbase + Cfg::kOffQ;
-  const uint32_t sDO = sbase + Cfg::kOffDO, sDS = sbase + Cfg::kOffDS;
+  const uint32_t sDO = sbase + Cfg::kOffDO, sDS = sbase + Cfg::kOffDS, sStage = sbase + Cfg::kOffStage;
   const uint32_t bars = sbase + Cfg::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT);
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(512, 1)
   // registers move from warpgroup 0 (producer, MMA) to the compute warpgroups at
   // the top of each warpgroup's branch
   if (warp < 4) {
-   regs_dec<Cfg::kRegsCtl>();
+   regs_set<Cfg::kRegsCtl, Cfg::kRegsLaunch>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
@@ -208,14 +212,18 @@ __global__ void __launch_bounds__(512, 1)
         const int nsteps = W[W_NQ];
         if (nsteps == 0) continue;
         if (!(ok = mbar_wait(bar(C_KVFULL), u & 1, abort_flag))) break;
-        for (int s = 0; s < nsteps && ok; ++s, ++sc) {
-          const int qs = sc & 1;
-          const uint32_t sQs = sQ + qs * Cfg::kTileBytes;
-          if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
-          tc_fence_after();
+        auto issue_s = [&](uint32_t step) {  // S^T = K Q^T for the Q tile of `step`
+          const uint32_t sQs = sQ + (step & 1) * Cfg::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmaj(sK, kk), kmaj(sQs, kk), idSS, kk > 0);
           tc_commit(bar(C_SFULL));
+        };
+        if (!(ok = mbar_wait(bar(C_QFULL0 + (sc & 1)), (sc >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_s(sc);
+        for (int s = 0; s < nsteps && ok; ++s, ++sc) {
+          const int qs = sc & 1;
+          const uint32_t sQs = sQ + qs * Cfg::kTileBytes;
           if (!(ok = mbar_wait(bar(C_DOFULL), sc & 1, abort_flag))) break;
           if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
@@ -231,6 +239,14 @@ __global__ void __launch_bounds__(512, 1)
             mma_ts(tmem + Cfg::kColDV, tmem + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), idKM,
                    (s > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(C_DOEMPTY));
+          // the next step's scores go ahead of this step's dK / dQ so that the
+          // P^T warps can start on them while the tensor core finishes this step
+          // (P^T of this step, in the same TMEM columns, was read by dV above)
+          if (s + 1 < nsteps) {
+            if (!(ok = mbar_wait(bar(C_QFULL0 + ((sc + 1) & 1)), ((sc + 1) >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_s(sc + 1);
+          }
           if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
           tc_fence_after();
 #pragma unroll
@@ -254,7 +270,7 @@ __global__ void __launch_bounds__(512, 1)
     }
    }
   } else if (warp < 12) {
-    regs_inc<Cfg::kRegsCompute>();
+    regs_set<Cfg::kRegsCompute, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ P^T / dS^T
     const int quarter = warp & 3, half = (warp - 4) >> 2;
     const int jl = quarter * 32 + lane;  // key row within the tile == TMEM lane
@@ -280,6 +296,10 @@ __global__ void __launch_bounds__(512, 1)
             if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
             if (!(ok = mbar_wait(bar(C_SFULL), sc & 1, abort_flag))) break;
             tc_fence_after();
+            // Rows' document starts are non-decreasing and invalid rows carry
+            // INT_MAX, so key j sees every query of the tile iff it lies at or
+            // before the tile's first row and at or after the last row's doc start.
+            const bool full = (j <= i0) && (j >= st_ds[127]);
             float p[64];
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
@@ -287,14 +307,23 @@ __global__ void __launch_bounds__(512, 1)
               tmem_ld32(tmem + lane_base + half * 64 + ch * 32, r);
               tmem_ld_wait();
               reg_fence(r);
-              uint32_t pk[16];
+              const int ib = half * 64 + ch * 32;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int i = half * 64 + ch * 32 + e;
-                const bool m = (j >= st_ds[i]) && (j <= i0 + i);
-                const float v = ex2(fmaf(__uint_as_float(r[e]), a.scale_log2, -st_lse[i]));
-                p[ch * 32 + e] = m ? v : 0.f;
+              for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 l4 = ld_shared_f4(st_lse + ib + 4 * e4);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  p[ch * 32 + 4 * e4 + k] = ex2(fmaf(__uint_as_float(r[4 * e4 + k]), a.scale_log2, -lv[k]));
               }
+              if (!full) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const int i = ib + e;
+                  if (!((j >= st_ds[i]) && (j <= i0 + i))) p[ch * 32 + e] = 0.f;
+                }
+              }
+              uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[ch * 32 + 2 * e], p[ch * 32 + 2 * e + 1]);
               tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk);
@@ -304,6 +333,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(bar(C_PREADY));
             if (!(ok = mbar_wait(bar(C_DPFULL), sc & 1, abort_flag))) break;
             tc_fence_after();
+            // dS^T of the previous step must have been consumed by its dK / dQ MMAs
+            if (sc > 0 && !(ok = mbar_wait(bar(C_DQFULL), (sc - 1) & 1, abort_flag))) break;
             const uint32_t row_addr = sDS + half * 16384 + jl * 128;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
@@ -311,13 +342,18 @@ __global__ void __launch_bounds__(512, 1)
               tmem_ld32(tmem + lane_base + Cfg::kColDP + half * 64 + ch * 32, r);
               tmem_ld_wait();
               reg_fence(r);
+              const int ib = half * 64 + ch * 32;
               uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int i = half * 64 + ch * 32 + 2 * e;
-                const float d0 = p[ch * 32 + 2 * e] * (__uint_as_float(r[2 * e]) - st_d[i]);
-                const float d1 = p[ch * 32 + 2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - st_d[i + 1]);
-                pk[e] = pack_bf16(d0, d1);
+              for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 d4 = ld_shared_f4(st_d + ib + 4 * e4);
+                const int e = 4 * e4;
+                const float s0 = p[ch * 32 + e] * (__uint_as_float(r[e]) - d4.x);
+                const float s1 = p[ch * 32 + e + 1] * (__uint_as_float(r[e + 1]) - d4.y);
+                const float s2 = p[ch * 32 + e + 2] * (__uint_as_float(r[e + 2]) - d4.z);
+                const float s3 = p[ch * 32 + e + 3] * (__uint_as_float(r[e + 3]) - d4.w);
+                pk[2 * e4] = pack_bf16(s0, s1);
+                pk[2 * e4 + 1] = pack_bf16(s2, s3);
               }
 #pragma unroll
               for (int c4 = 0; c4 < 4; ++c4) {
@@ -332,11 +368,12 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
   } else {
-    regs_inc<Cfg::kRegsDq>();
+    regs_set<Cfg::kRegsDq, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ dQ out, dK/dV epilogue
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // query row (dQ) or key row (dK/dV) == TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const uint32_t stg_row = sStage + rl * 128;
     uint32_t u = 0, sc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
@@ -367,25 +404,40 @@ __global__ void __launch_bounds__(512, 1)
             const int h = g * a.G + hh;
             const int lrow = t * 128 + rl;
             const bool qrow_ok = lrow < a.L && r0 + lrow < svalid;
-            float* dqrow = a.dq + b * a.q_sb + c * a.q_sc + int64_t(lrow) * a.q_sr + int64_t(h) * a.q_sh;
-            if (!(ok = mbar_wait(bar(C_DQFULL), sc & 1, abort_flag))) break;
+            // the warpgroup meets at named barriers below: leave together or not at all
+            ok = bar_red_and(1, 128, mbar_wait(bar(C_DQFULL), sc & 1, abort_flag));
+            if (!ok) break;
             tc_fence_after();
+            // dQ tile (128 query rows x D fp32) goes to global memory as D/32
+            // reduce-adds of 128 x 32 boxes staged through shared memory in the
+            // 128-byte-swizzled layout (rows past L are clipped by the map).
 #pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
               uint32_t r[32];
               tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r);
               tmem_ld_wait();
               reg_fence(r);
-              if (qrow_ok) {
+              if (q == D / 32 - 1) {
+                tc_fence_before();
+                mbar_arrive(bar(C_DQEMPTY));
+              }
+              if (rl == 0) bulk_wait_read<0>();  // the previous box has left the staging tile
+              named_bar_sync(1, 128);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  red_add_v4(dqrow + q * 32 + 4 * e, __uint_as_float(r[4 * e]) * a.scale,
-                             __uint_as_float(r[4 * e + 1]) * a.scale, __uint_as_float(r[4 * e + 2]) * a.scale,
-                             __uint_as_float(r[4 * e + 3]) * a.scale);
+              for (int c16 = 0; c16 < 8; ++c16)
+                st_shared_v4(stg_row + ((c16 ^ (rl & 7)) << 4), __float_as_uint(__uint_as_float(r[4 * c16]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[4 * c16 + 1]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[4 * c16 + 2]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[4 * c16 + 3]) * a.scale));
+              fence_proxy_async_smem();
+              named_bar_sync(1, 128);
+              if (rl == 0) {
+                tma_reduce_add_5d(&tm_dq, sStage, q * 32, h, t * 128, c, b);
+                bulk_commit();
               }
             }
-            tc_fence_before();
-            mbar_arrive(bar(C_DQEMPTY));
+            (void)lrow;
+            (void)svalid;
           }
       }
       if (!ok) break;
@@ -423,6 +475,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_arrive(bar(C_ACCEMPTY));
       ++u;
     }
+    if (rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
   }
 
   tc_fence_before();
@@ -439,7 +492,8 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int D>
 static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                          const CUtensorMap& mdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+                          const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdArgs& a, int grid,
+                          cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -450,12 +504,13 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, bd_bwd_kernel<D>);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd)");
-    if (fa.numRegs * Cfg::kThreads < Cfg::kRegsNeeded)
-      return fail(BD_ERR_UNSUPPORTED, "bwd kernel built with %d registers/thread, register split needs %d",
-                  fa.numRegs, (Cfg::kRegsNeeded + Cfg::kThreads - 1) / Cfg::kThreads);
+    // the setmaxnreg directions were chosen for this launch count: refuse any other
+    if (fa.numRegs != Cfg::kRegsLaunch)
+      return fail(BD_ERR_UNSUPPORTED, "bwd kernel built with %d registers/thread, its register split assumes %d",
+                  fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
-  bd_bwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, a);
+  bd_bwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, mdq, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_bwd_kernel launch");
   return BD_OK;
@@ -542,7 +597,7 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, true))) return st;
   if ((st = check_tensor(k, "k", 2, c.B, c.Ck, c.Hkv, true))) return st;
   if ((st = check_tensor(v, "v", 2, c.B, c.Ck, c.Hkv, true))) return st;
-  if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, false))) return st;
+  if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, true))) return st;
   if ((st = check_tensor(dk, "dk", 4, c.B, c.Ck, c.Hkv, false))) return st;
   if ((st = check_tensor(dv, "dv", 4, c.B, c.Ck, c.Hkv, false))) return st;
   if (q->rows != c.L || dout->rows != c.L || dq->rows != c.L)
@@ -551,7 +606,8 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
     return fail(BD_ERR_ARG, "k/v rows < %d needed by the plan", pv.hdr(H_KV_ROWS));
   if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
   if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  if ((st = make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq"))) return st;
   if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q"))) return st;
   if ((st = make_tmap_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout"))) return st;
   if ((st = make_tmap_bf16(&mk, k, c.B, c.Ck, c.Hkv, c.D, "k"))) return st;
@@ -580,7 +636,8 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   if ((st = sm_count(&nsm))) return st;
   const int grid = a.n_work < nsm ? a.n_work : nsm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = c.D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, a, grid, s) : launch_bwd<64>(mq, mk, mv, mdo, a, grid, s);
+  st = c.D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, mdq, a, grid, s)
+                  : launch_bwd<64>(mq, mk, mv, mdo, mdq, a, grid, s);
   if (st) return st;
   return ok();
 }

@@ -59,6 +59,8 @@ struct FwdCfg {
   // softmax warpgroups; the sum must fit in what the launch reserved
   static constexpr int kRegsCtl = 72, kRegsSoftmax = 216;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
+  static constexpr int kRegsLaunch = 168;  // 65536 / 384 threads, rounded down to 8
+  static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
 };
 
 // barrier indices (8 bytes each)
@@ -66,18 +68,6 @@ enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 6, B_KVEMPTY = 10, B_SFULL = 14, B_PFULL = 16,
   B_OFINAL = 18, B_OEMPTY = 20, B_DRAIN = 22, B_COUNT = 23
 };
-
-__device__ __forceinline__ int find_doc_start(const int32_t* segs, int nseg, int row) {
-  int lo = 0, hi = nseg - 1;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    const int32_t* g = segs + mid * kSegWords;
-    if (row < g[1]) hi = mid - 1;
-    else if (row >= g[1] + g[2]) lo = mid + 1;
-    else return g[3];
-  }
-  return -1;
-}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -99,7 +89,7 @@ __global__ void __launch_bounds__(384, 1)
   const int32_t* plan = a.plan;
   const int32_t* work = plan + plan[H_OFF_FWD];
   const int32_t* items = plan + plan[H_OFF_ITEMS];
-  const int32_t* segs_all = plan + plan[H_OFF_SEGS];
+  const int32_t* rowds_all = plan + plan[H_OFF_ROWDS];
   const int slots = a.slots;
 
   if (threadIdx.x == 0) {
@@ -131,7 +121,7 @@ __global__ void __launch_bounds__(384, 1)
   // the softmax warpgroups hold a 128-column score row each: registers move to
   // them from warpgroup 0 (producer and MMA warps) at the top of each branch
   if (warp < 4) {
-   regs_dec<Cfg::kRegsCtl>();
+   regs_set<Cfg::kRegsCtl, Cfg::kRegsLaunch>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
@@ -253,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
     }
    }
   } else {
-    regs_inc<Cfg::kRegsSoftmax>();
+    regs_set<Cfg::kRegsSoftmax, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ softmax
     const int s = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -273,9 +263,9 @@ __global__ void __launch_bounds__(384, 1)
         const int lrow = W[F_QTILE] * 128 + r;  // row within the chunk
         const int grow = I[I_ROW0] + lrow;      // global row
         const bool row_ok = lrow < a.L;
-        int ds = -1;
-        if (row_ok && grow < I[I_SVALID]) ds = find_doc_start(segs_all + I[I_SEG0] * kSegWords, I[I_NSEG], grow);
-        const bool valid = ds >= 0;
+        const int ds = row_ok ? rowds_all[W[F_ITEM] * a.L + lrow] : kRowInvalid;
+        const bool valid = ds != kRowInvalid;
+        (void)grow;
         __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(lrow) * a.o_sr + int64_t(h) * a.o_sh;
         float* lrow_p = a.lse + b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + lrow;
         if (nt == 0) {
@@ -311,9 +301,15 @@ __global__ void __launch_bounds__(384, 1)
               if (!(valid && col >= ds && col <= grow)) x[e] = -CUDART_INF_F;
             }
           }
-          float mx = x[0];
+          // row max: eight independent 3-input max chains, then a small tree
+          float m8[8];
 #pragma unroll
-          for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(x[k], x[8 + k]);
+#pragma unroll
+          for (int e = 16; e < 128; e += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], x[e + k], x[e + 8 + k]);
+          const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
           const float m_new = fmaxf(m_run, mx * a.scale_log2);
           const bool need = m_new > m_run + 8.0f;
           float factor = 1.f;
@@ -335,15 +331,23 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           const float m_eff = (m_run == -CUDART_INF_F) ? 0.f : m_run;
-          float sum = 0.f;
+          // p = 2^(x * scale_log2 - m): paired FMAs, then the exponentials; the
+          // row sum uses four paired accumulators
+          const float2 cs = make_float2(a.scale_log2, a.scale_log2), cm = make_float2(-m_eff, -m_eff);
+          float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
           uint32_t pk[2][32];
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
-            const float p0 = ex2(fmaf(x[2 * e], a.scale_log2, -m_eff));
-            const float p1 = ex2(fmaf(x[2 * e + 1], a.scale_log2, -m_eff));
-            sum += p0 + p1;
-            pk[e >> 5][e & 31] = pack_bf16(p0, p1);
+            float2 t = ffma2(make_float2(x[2 * e], x[2 * e + 1]), cs, cm);
+            t.x = ex2(t.x);
+            t.y = ex2(t.y);
+            s4[e & 3] = fadd2(s4[e & 3], t);
+            pk[e >> 5][e & 31] = pack_bf16(t.x, t.y);
           }
+          const float2 s01 = fadd2(s4[0], s4[1]), s23 = fadd2(s4[2], s4[3]);
+          const float2 st = fadd2(s01, s23);
+          const float sum = st.x + st.y;
           l_run += sum;
           tmem_st32(tS, pk[0]);
           tmem_st32(tS + 32, pk[1]);
@@ -405,9 +409,9 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
     e = cudaFuncGetAttributes(&fa, bd_fwd_kernel<D>);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
     // setmaxnreg.inc waits until registers are free: never launch a split that cannot be met
-    if (fa.numRegs * Cfg::kThreads < Cfg::kRegsNeeded)
-      return fail(BD_ERR_UNSUPPORTED, "fwd kernel built with %d registers/thread, register split needs %d",
-                  fa.numRegs, (Cfg::kRegsNeeded + Cfg::kThreads - 1) / Cfg::kThreads);
+    if (fa.numRegs != Cfg::kRegsLaunch)
+      return fail(BD_ERR_UNSUPPORTED, "fwd kernel built with %d registers/thread, its register split assumes %d",
+                  fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
   bd_fwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);

@@ -1,7 +1,8 @@
 // Small HBM-bound kernels around the backward main loop, plus status readback.
 //
 //   bd_bwd_pre_kernel   D_i = <dO_i, O_i> in fp32 for every (row, head) of every
-//                       chunk, and zeroes the fp32 dQ accumulator rows.
+//                       chunk, the log2-domain LSE and each row's document
+//                       start, and zeroes the fp32 dQ accumulator rows.
 //   bd_owner_sum_kernel adds needed-only-window dK/dV partials into the rows'
 //                       owners, chunk by chunk in plan order (deterministic);
 //                       the single-GPU form of the index_add / reduce-scatter
@@ -28,81 +29,75 @@ BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
   return w;
 }
 
-__device__ __forceinline__ int doc_start_of(const int32_t* segs, int nseg, int row) {
-  int lo = 0, hi = nseg - 1;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    const int32_t* g = segs + mid * kSegWords;
-    if (row < g[1]) hi = mid - 1;
-    else if (row >= g[1] + g[2]) lo = mid + 1;
-    else return g[3];
-  }
-  return -1;
-}
-
-// One warp per (item, row < Lpad, head): D, log2-domain LSE, the row's document
-// start (head 0 only), and zeroing of the dQ accumulator row.
+// One block per (item, row < Lpad): D for every head, the log2-domain LSE, the
+// row's document start, and zeroing of the row's dQ accumulator. Threads take
+// 16-byte pieces of O / dO (all heads of the row); a head's pieces sit in
+// consecutive lanes and are summed with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
-  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = int64_t(a.nitems) * a.Lpad * a.H;
-  if (wid >= total) return;
-  const int h = int(wid % a.H);
-  const int l = int((wid / a.H) % a.Lpad);
-  const int item = int(wid / (int64_t(a.H) * a.Lpad));
+  const int item = blockIdx.x / a.Lpad, l = blockIdx.x % a.Lpad;
   const int b = item / a.C, c = item % a.C;
-  const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+  const int tid = threadIdx.x;
+  constexpr int CPH = D / 8;  // 16-byte pieces per head (8 or 16: groups never straddle a warp)
+  const float inf = __int_as_float(0x7f800000);
   if (l >= a.L) {
-    if (lane == 0) {
-      a.lse2[sidx] = __int_as_float(0x7f800000);
+    for (int h = tid; h < a.H; h += blockDim.x) {
+      const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+      a.lse2[sidx] = inf;
       a.dstat[sidx] = 0.f;
-      if (h == 0) a.rowds[int64_t(item) * a.Lpad + l] = 0x7fffffff;
     }
+    if (tid == 0) a.rowds[int64_t(item) * a.Lpad + l] = 0x7fffffff;
     return;
   }
-  const int32_t* I = a.plan + a.plan[H_OFF_ITEMS] + item * kItemWords;
-  const int grow = I[I_ROW0] + l;
-  int ds = -1;
-  if (grow < I[I_SVALID]) ds = doc_start_of(a.plan + a.plan[H_OFF_SEGS] + I[I_SEG0] * kSegWords, I[I_NSEG], grow);
-  constexpr int PER = D / 32;  // bf16 values per lane
-  const __nv_bfloat16* o = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr + int64_t(h) * a.o_sh + lane * PER;
-  const __nv_bfloat16* g = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr + int64_t(h) * a.g_sh + lane * PER;
-  float acc = 0.f;
-  if (PER == 4) {
-    const uint2 ov = *reinterpret_cast<const uint2*>(o);
-    const uint2 gv = *reinterpret_cast<const uint2*>(g);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+  __shared__ int s_ds;
+  if (tid == 0) {
+    const int32_t v = a.plan[a.plan[H_OFF_ROWDS] + item * a.L + l];
+    s_ds = v == kRowInvalid ? -1 : v;
+    a.rowds[int64_t(item) * a.Lpad + l] = v;
+  }
+  __syncthreads();
+  const int ds = s_ds;
+  const __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr;
+  const __nv_bfloat16* grow_p = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr;
+  const int npieces = a.H * CPH;
+  const int nround = (npieces + 255) & ~255;
+  for (int k0 = 0; k0 < nround; k0 += 256) {
+    const int k = k0 + tid;
+    const bool act = k < npieces;
+    const int h = k / CPH, col = (k % CPH) * 8;
+    float acc = 0.f;
+    if (act) {
+      const uint4 ov = *reinterpret_cast<const uint4*>(orow + int64_t(h) * a.o_sh + col);
+      const uint4 gv = *reinterpret_cast<const uint4*>(grow_p + int64_t(h) * a.g_sh + col);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      }
     }
-  } else {
-    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o);
-    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g);
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv));
-    acc = fmaf(x.x, y.x, x.y * y.y);
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    a.dstat[sidx] = ds >= 0 ? acc : 0.f;
-    const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
-    a.lse2[sidx] = ds >= 0 ? lse * 1.4426950408889634f : __int_as_float(0x7f800000);
-    if (h == 0) a.rowds[int64_t(item) * a.Lpad + l] = ds >= 0 ? ds : 0x7fffffff;
+    for (int off = CPH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (act && (k % CPH) == 0) {
+      const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+      a.dstat[sidx] = ds >= 0 ? acc : 0.f;
+      const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
+      a.lse2[sidx] = ds >= 0 ? lse * 1.4426950408889634f : inf;
+    }
   }
-  float* dq = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + lane * PER;
-  if (PER == 4) *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
-  else *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+  float* dqrow = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = tid; k < a.H * (D / 4); k += 256) {
+    const int h = k / (D / 4), col = (k % (D / 4)) * 4;
+    *reinterpret_cast<float4*>(dqrow + int64_t(h) * a.q_sh + col) = z;
+  }
 }
 
 int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
-  const int64_t warps = int64_t(a.nitems) * a.Lpad * a.H;
-  const int64_t blocks = (warps * 32 + 255) / 256;
+  const int64_t blocks = int64_t(a.nitems) * a.Lpad;
   if (blocks == 0) return BD_OK;
+  if (blocks > 0x7fffffff) return fail(BD_ERR_UNSUPPORTED, "too many rows for the statistics kernel");
   if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);
   else bd_bwd_pre_kernel<64><<<unsigned(blocks), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();

@@ -44,27 +44,35 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
-                       const char* name) {
+static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                         const char* name, int esize, CUtensorMapDataType dtype, cuuint32_t box0) {
   auto fn = encode_fn();
   if (!fn) return fail(BD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
-  // Extent-1 dims may carry any stride; give them a valid one.
-  auto fix = [](int64_t stride_elems, int64_t ext, int64_t fallback) {
-    return ext <= 1 ? fallback : stride_elems * 2;
+  auto fix = [esize](int64_t stride_elems, int64_t ext, int64_t fallback) {
+    return ext <= 1 ? fallback : stride_elems * esize;
   };
-  const int64_t sh = fix(t->stride_head, heads, d * 2);
+  const int64_t sh = fix(t->stride_head, heads, d * esize);
   const int64_t sr = fix(t->stride_row, t->rows, sh * heads);
   const int64_t sc = fix(t->stride_c, C, sr * t->rows);
   const int64_t sb = fix(t->stride_b, B, sc * C);
   cuuint64_t dims[5] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(t->rows), cuuint64_t(C), cuuint64_t(B)};
   cuuint64_t strides[4] = {cuuint64_t(sh), cuuint64_t(sr), cuuint64_t(sc), cuuint64_t(sb)};
-  cuuint32_t box[5] = {64, 1, 128, 1, 1};
+  cuuint32_t box[5] = {box0, 1, 128, 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, t->ptr, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dtype, 5, t->ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(BD_ERR_ALIGN, "%s: cuTensorMapEncodeTiled failed (%d)", name, int(r));
   return BD_OK;
+}
+
+int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                             const char* name) {
+  return make_tmap(map, t, B, C, heads, d, name, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32);
+}
+
+int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                       const char* name) {
+  return make_tmap(map, t, B, C, heads, d, name, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64);
 }
 
 int32_t sm_count(int* out) {

@@ -20,6 +20,11 @@ int32_t check_tensor(const bd_tensor* t, const char* name, int elem_bytes, int64
 int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads,
                        int64_t d, const char* name);
 
+// Encodes a 5-D tiled TMA map over fp32 [B, C, rows, heads, d] with a box of
+// 128 rows x 32 columns of one head, 128-byte swizzle (for reduce-adds).
+int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                             const char* name);
+
 // Number of SMs of the current device (cached per device).
 int32_t sm_count(int* out);
 

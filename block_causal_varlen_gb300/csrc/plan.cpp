@@ -56,7 +56,8 @@ int32_t view_plan(const void* plan_host, PlanView* out) {
     return off >= kHdrWords && n >= 0 && off + n * stride <= words;
   };
   if (!in(w[H_OFF_ITEMS], w[H_NITEMS], kItemWords) || !in(w[H_OFF_SEGS], w[H_NSEGS], kSegWords) ||
-      !in(w[H_OFF_FWD], w[H_NFWD], kFwdWords) || !in(w[H_OFF_BWD], w[H_NBWD], kBwdWords))
+      !in(w[H_OFF_FWD], w[H_NFWD], kFwdWords) || !in(w[H_OFF_BWD], w[H_NBWD], kBwdWords) ||
+      !in(w[H_OFF_ROWDS], w[H_NITEMS], w[H_L]))
     return fail(BD_ERR_PLAN, "plan blob offsets are inconsistent");
   out->w = w;
   return BD_OK;
@@ -132,7 +133,7 @@ extern "C" int32_t bd_segment(const int32_t* cu, int32_t ndocs, int32_t S, int32
 namespace {
 
 struct Built {
-  std::vector<int32_t> items, segs, fwd, bwd;
+  std::vector<int32_t> items, segs, fwd, bwd, rowds;
   int64_t useful = 0, fwd_tiles = 0;
   int32_t kv_rows = 0, slots = 1, qtiles = 0, nbuf = 0, C = 0, Ck = 1;
 };
@@ -203,6 +204,14 @@ int32_t build(const bd_plan_desc* d, Built* out) {
         P.segs.insert(P.segs.end(), w, w + kSegWords);
       }
       P.kv_rows = std::max(P.kv_rows, d->kv_mode == BD_KV_GATHER ? h.s_valid : h.kv_end - h.kv_start);
+      // per-row document start: segments cover the chunk's valid rows in order
+      {
+        const size_t base = P.rowds.size();
+        P.rowds.resize(base + L, kRowInvalid);
+        for (int32_t s = 0; s < h.nseg; ++s)
+          for (int32_t r = tmp[s].q_start; r < tmp[s].q_start + tmp[s].q_len; ++r)
+            P.rowds[base + (r - h.row_offset)] = tmp[s].k_start;
+      }
     }
   }
   // ---- forward work: (item, query tile, head slot group), longest first -------------
@@ -271,14 +280,22 @@ int32_t build(const bd_plan_desc* d, Built* out) {
       }
     }
   }
-  std::stable_sort(bw.begin(), bw.end(), [](const BW& x, const BW& y) { return x.w[W_NQ] > y.w[W_NQ]; });
+  // Units of one (K/V head, K/V buffer) read the same Q / dO tiles and add into the
+  // same dQ tiles: keep them together so that the CTAs running at the same time
+  // share those tiles in L2; longest first within a group.
+  std::stable_sort(bw.begin(), bw.end(), [](const BW& x, const BW& y) {
+    if (x.w[W_G] != y.w[W_G]) return x.w[W_G] < y.w[W_G];
+    if (x.w[W_BUF] != y.w[W_BUF]) return x.w[W_BUF] < y.w[W_BUF];
+    return x.w[W_NQ] > y.w[W_NQ];
+  });
   for (const BW& w : bw) P.bwd.insert(P.bwd.end(), w.w, w.w + kBwdWords);
   return BD_OK;
 }
 
 size_t words_of(const Built& P) {
   auto al = [](size_t x) { return (x + 3) & ~size_t(3); };  // keep 16-byte alignment per section
-  return kHdrWords + al(P.items.size()) + al(P.segs.size()) + al(P.fwd.size()) + al(P.bwd.size());
+  return kHdrWords + al(P.items.size()) + al(P.segs.size()) + al(P.fwd.size()) + al(P.bwd.size()) +
+         al(P.rowds.size());
 }
 
 }  // namespace
@@ -320,6 +337,8 @@ extern "C" int32_t bd_plan_build(const bd_plan_desc* d, void* blob, size_t blob_
   std::copy(P.fwd.begin(), P.fwd.end(), w + off); off += al(P.fwd.size());
   w[H_OFF_BWD] = off; w[H_NBWD] = int32_t(P.bwd.size() / kBwdWords);
   std::copy(P.bwd.begin(), P.bwd.end(), w + off); off += al(P.bwd.size());
+  w[H_OFF_ROWDS] = off;
+  std::copy(P.rowds.begin(), P.rowds.end(), w + off); off += al(P.rowds.size());
   w[H_SCALE_BITS] = scale_bits; w[H_KV_ROWS] = P.kv_rows; w[H_CK] = P.Ck; w[H_SLOTS] = P.slots;
   w[H_QTILES] = P.qtiles;
   w[H_USEFUL_LO] = int32_t(P.useful & 0x7fffffff); w[H_USEFUL_HI] = int32_t(P.useful >> 31);

@@ -16,6 +16,8 @@ enum : int {
   H_KVMODE, H_G, H_NITEMS, H_OFF_ITEMS, H_OFF_SEGS, H_NSEGS, H_OFF_FWD, H_NFWD,
   H_OFF_BWD, H_NBWD, H_SCALE_BITS, H_KV_ROWS, H_CK, H_SLOTS, H_QTILES,
   H_USEFUL_LO, H_USEFUL_HI, H_NBUF, H_FWD_TILES_LO, H_FWD_TILES_HI,
+  H_OFF_ROWDS,          // int32 [nitems][L]: global start row of each chunk row's
+                        // document, kRowInvalid for padding rows
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
   H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
   kHdrWords = 64
@@ -29,6 +31,8 @@ enum : int {
   I_USEFUL_LO, I_USEFUL_HI, I_RESERVED0, I_RESERVED1,
   kItemWords = 16
 };
+
+constexpr int32_t kRowInvalid = 0x7fffffff;
 
 constexpr int kSegWords = 6;  // doc, q_start, q_len, k_start, k_len, diag_off
 

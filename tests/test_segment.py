@@ -186,3 +186,21 @@ def test_plan_rejects_bad_desc():
         lib.Plan([[0, 100]], 100, 2, 4, 4, 96)            # head dim
     with pytest.raises(lib.BDError):
         lib.Plan([[0, 100]], 100, 2, 4, 4, 64, ranks=[0, 2])  # rank out of range
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("i", [1, 2, 3, 5])
+def test_plan_row_doc_starts_match_oracle(i):
+    """The per-row document starts the kernels read from the plan equal the
+    first index of each row's document id (padding rows: 2**31 - 1)."""
+    wl = workloads.config(i)
+    plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d)
+    got = plan.row_doc_starts()
+    for b, cu in enumerate(wl.cu):
+        ids = oracle.doc_ids(cu, wl.S)
+        first = {}
+        for t, x in enumerate(ids):
+            if x >= 0 and x not in first:
+                first[x] = t
+        want = np.array([first[x] if x >= 0 else 2 ** 31 - 1 for x in ids], dtype=np.int64)
+        assert np.array_equal(got[b * wl.cp:(b + 1) * wl.cp].reshape(-1).astype(np.int64), want)
