@@ -87,6 +87,7 @@ EXPORTS = {
     "bd_owner_sum": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                  C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_void_p]),
     "bd_check_status": (C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p]),
+    "bd_selftest_bounded_wait": (C.c_int32, [C.c_void_p, C.c_uint32, C.c_void_p]),
     "bd_last_error": (C.c_char_p, []),
     "bd_version": (C.c_int32, []),
 }

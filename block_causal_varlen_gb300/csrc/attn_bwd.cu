@@ -71,7 +71,7 @@ struct BwdCfg {
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
-  static constexpr int kRegsCtl = 88, kRegsCompute = 144, kRegsDq = 112;
+  static constexpr int kRegsCtl = 88, kRegsCompute = 128, kRegsDq = 168;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
   static constexpr int kRegsLaunch = 128;  // 65536 / 512 threads: what ptxas assigns at launch
   static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
@@ -249,13 +249,14 @@ __global__ void __launch_bounds__(512, 1)
           }
           if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
           tc_fence_after();
+          // dQ first: its drain gates the next step's dP^T (same TMEM columns)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + Cfg::kColDP, mnmaj(sDS, kk), mnmaj(sK, kk), idMM, kk > 0);
+          tc_commit(bar(C_DQFULL));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + Cfg::kColDK, kmaj(sDS, kk), mnmaj(sQs, kk), idKM, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + Cfg::kColDP, mnmaj(sDS, kk), mnmaj(sK, kk), idMM, kk > 0);
-          tc_commit(bar(C_QEMPTY0 + qs));
-          tc_commit(bar(C_DQFULL));
+          tc_commit(bar(C_QEMPTY0 + qs));  // Q and dS^T of this step are free after dK
           if (s == nsteps - 1) {
             tc_commit(bar(C_ACCDONE));
             tc_commit(bar(C_KVEMPTY));
@@ -300,7 +301,9 @@ __global__ void __launch_bounds__(512, 1)
             // INT_MAX, so key j sees every query of the tile iff it lies at or
             // before the tile's first row and at or after the last row's doc start.
             const bool full = (j <= i0) && (j >= st_ds[127]);
-            float p[64];
+            // P^T is kept as the bf16 pairs written to TMEM (the dV MMA reads the same
+            // rounded values); dS below unpacks them
+            uint32_t pk[2][16];
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
               uint32_t r[32];
@@ -308,33 +311,35 @@ __global__ void __launch_bounds__(512, 1)
               tmem_ld_wait();
               reg_fence(r);
               const int ib = half * 64 + ch * 32;
+              float p[32];
 #pragma unroll
               for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 l4 = ld_shared_f4(st_lse + ib + 4 * e4);
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  p[ch * 32 + 4 * e4 + k] = ex2(fmaf(__uint_as_float(r[4 * e4 + k]), a.scale_log2, -lv[k]));
+                  p[4 * e4 + k] = ex2(fmaf(__uint_as_float(r[4 * e4 + k]), a.scale_log2, -lv[k]));
               }
               if (!full) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                   const int i = ib + e;
-                  if (!((j >= st_ds[i]) && (j <= i0 + i))) p[ch * 32 + e] = 0.f;
+                  if (!((j >= st_ds[i]) && (j <= i0 + i))) p[e] = 0.f;
                 }
               }
-              uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[ch * 32 + 2 * e], p[ch * 32 + 2 * e + 1]);
-              tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk);
+              for (int e = 0; e < 16; ++e) pk[ch][e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+              tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk[ch]);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(C_PREADY));
             if (!(ok = mbar_wait(bar(C_DPFULL), sc & 1, abort_flag))) break;
             tc_fence_after();
-            // dS^T of the previous step must have been consumed by its dK / dQ MMAs
-            if (sc > 0 && !(ok = mbar_wait(bar(C_DQFULL), (sc - 1) & 1, abort_flag))) break;
+            // dS^T of the previous step must have been consumed by its dQ and dK MMAs
+            // (dK is the later one; its commit also releases that step's Q stage)
+            if (sc > 0 && !(ok = mbar_wait(bar(C_QEMPTY0 + ((sc - 1) & 1)), ((sc - 1) >> 1) & 1, abort_flag)))
+              break;
             const uint32_t row_addr = sDS + half * 16384 + jl * 128;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
@@ -343,23 +348,24 @@ __global__ void __launch_bounds__(512, 1)
               tmem_ld_wait();
               reg_fence(r);
               const int ib = half * 64 + ch * 32;
-              uint32_t pk[16];
+              uint32_t dsk[16];
 #pragma unroll
               for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 d4 = ld_shared_f4(st_d + ib + 4 * e4);
                 const int e = 4 * e4;
-                const float s0 = p[ch * 32 + e] * (__uint_as_float(r[e]) - d4.x);
-                const float s1 = p[ch * 32 + e + 1] * (__uint_as_float(r[e + 1]) - d4.y);
-                const float s2 = p[ch * 32 + e + 2] * (__uint_as_float(r[e + 2]) - d4.z);
-                const float s3 = p[ch * 32 + e + 3] * (__uint_as_float(r[e + 3]) - d4.w);
-                pk[2 * e4] = pack_bf16(s0, s1);
-                pk[2 * e4 + 1] = pack_bf16(s2, s3);
+                const uint32_t p01 = pk[ch][2 * e4], p23 = pk[ch][2 * e4 + 1];
+                const float s0 = __uint_as_float(p01 << 16) * (__uint_as_float(r[e]) - d4.x);
+                const float s1 = __uint_as_float(p01 & 0xffff0000u) * (__uint_as_float(r[e + 1]) - d4.y);
+                const float s2 = __uint_as_float(p23 << 16) * (__uint_as_float(r[e + 2]) - d4.z);
+                const float s3 = __uint_as_float(p23 & 0xffff0000u) * (__uint_as_float(r[e + 3]) - d4.w);
+                dsk[2 * e4] = pack_bf16(s0, s1);
+                dsk[2 * e4 + 1] = pack_bf16(s2, s3);
               }
 #pragma unroll
               for (int c4 = 0; c4 < 4; ++c4) {
                 const int chunk = ch * 4 + c4;  // 16-byte chunk of the 128-byte row
-                st_shared_v4(row_addr + ((chunk ^ (jl & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2],
-                             pk[4 * c4 + 3]);
+                st_shared_v4(row_addr + ((chunk ^ (jl & 7)) << 4), dsk[4 * c4], dsk[4 * c4 + 1], dsk[4 * c4 + 2],
+                             dsk[4 * c4 + 3]);
               }
             }
             fence_proxy_async_smem();
@@ -411,24 +417,26 @@ __global__ void __launch_bounds__(512, 1)
             // dQ tile (128 query rows x D fp32) goes to global memory as D/32
             // reduce-adds of 128 x 32 boxes staged through shared memory in the
             // 128-byte-swizzled layout (rows past L are clipped by the map).
-#pragma unroll 1
+            // the whole dQ row leaves TMEM first, so the next dP^T can start at once
+            uint32_t r[D / 32][32];
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r[q]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) reg_fence(r[q]);
+            tc_fence_before();
+            mbar_arrive(bar(C_DQEMPTY));
+#pragma unroll
             for (int q = 0; q < D / 32; ++q) {
-              uint32_t r[32];
-              tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r);
-              tmem_ld_wait();
-              reg_fence(r);
-              if (q == D / 32 - 1) {
-                tc_fence_before();
-                mbar_arrive(bar(C_DQEMPTY));
-              }
               if (rl == 0) bulk_wait_read<0>();  // the previous box has left the staging tile
               named_bar_sync(1, 128);
 #pragma unroll
               for (int c16 = 0; c16 < 8; ++c16)
-                st_shared_v4(stg_row + ((c16 ^ (rl & 7)) << 4), __float_as_uint(__uint_as_float(r[4 * c16]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[4 * c16 + 1]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[4 * c16 + 2]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[4 * c16 + 3]) * a.scale));
+                st_shared_v4(stg_row + ((c16 ^ (rl & 7)) << 4),
+                             __float_as_uint(__uint_as_float(r[q][4 * c16]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 1]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 2]) * a.scale),
+                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 3]) * a.scale));
               fence_proxy_async_smem();
               named_bar_sync(1, 128);
               if (rl == 0) {

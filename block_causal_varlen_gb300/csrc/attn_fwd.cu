@@ -47,11 +47,14 @@ struct FwdArgs {
 template <int D>
 struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K and V have rings of their own: a K tile is released as soon as both
+  // slots' S MMAs have read it, so it can be refilled well ahead of its use.
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr int kOCol = 256;                   // first O column in TMEM
   static constexpr int kThreads = 384;
@@ -65,8 +68,8 @@ struct FwdCfg {
 
 // barrier indices (8 bytes each)
 enum : int {
-  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 6, B_KVEMPTY = 10, B_SFULL = 14, B_PFULL = 16,
-  B_OFINAL = 18, B_OEMPTY = 20, B_DRAIN = 22, B_COUNT = 23
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14, B_SFULL = 18,
+  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_COUNT = 27
 };
 
 template <int D>
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(384, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using Cfg = FwdCfg<D>;
-  constexpr int NST = Cfg::kStages;
+  constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -95,10 +98,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < NST; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t kv_it = 0, qi = 0;
+      uint32_t k_it = 0, v_it = 0, qi = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
         const int32_t* W = work + w * kFwdWords;
@@ -145,29 +151,35 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_5d(sQ + s * Cfg::kTileBytes + hf * 16384, &tm_q, bar(B_QFULL), hf * 64, W[F_H0] + s,
                         W[F_QTILE] * 128, c, b);
         ++qi;
-        for (int j = 0; j < nt; ++j, ++kv_it) {
-          const int st = kv_it % NST;
-          if (!(ok = mbar_wait(bar(B_KVEMPTY + st), ((kv_it / NST) & 1) ^ 1, abort_flag))) break;
+        for (int j = 0; j < nt; ++j) {
           const int row = (W[F_KTLO] + j) * 128 - kvbase;
-          mbar_expect_tx(bar(B_KFULL + st), Cfg::kTileBytes);
+          const int sk = k_it % NK, sv = v_it % NV;
+          if (!(ok = mbar_wait(bar(B_KEMPTY + sk), ((k_it / NK) & 1) ^ 1, abort_flag))) break;
+          mbar_expect_tx(bar(B_KFULL + sk), Cfg::kTileBytes);
           for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_5d(sK + st * Cfg::kTileBytes + hf * 16384, &tm_k, bar(B_KFULL + st), hf * 64, g, row, kc,
+            tma_load_5d(sK + sk * Cfg::kTileBytes + hf * 16384, &tm_k, bar(B_KFULL + sk), hf * 64, g, row, kc,
                         kb);
-          mbar_expect_tx(bar(B_VFULL + st), Cfg::kTileBytes);
+          ++k_it;
+          if (!(ok = mbar_wait(bar(B_VEMPTY + sv), ((v_it / NV) & 1) ^ 1, abort_flag))) break;
+          mbar_expect_tx(bar(B_VFULL + sv), Cfg::kTileBytes);
           for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_5d(sV + st * Cfg::kTileBytes + hf * 16384, &tm_v, bar(B_VFULL + st), hf * 64, g, row, kc,
+            tma_load_5d(sV + sv * Cfg::kTileBytes + hf * 16384, &tm_v, bar(B_VFULL + sv), hf * 64, g, row, kc,
                         kb);
+          ++v_it;
         }
       }
       if (!ok) {
         // let every copy already issued land before the CTA's shared memory goes away
-        for (int s = 0; s < NST; ++s) {
-          if (kv_it > uint32_t(s)) {
-            const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % NST);
-            mbar_wait_drain(bar(B_KFULL + s), (last / NST) & 1);
-            mbar_wait_drain(bar(B_VFULL + s), (last / NST) & 1);
+        for (int s = 0; s < NK; ++s)
+          if (k_it > uint32_t(s)) {
+            const uint32_t last = k_it - 1 - ((k_it - 1 - s) % NK);
+            mbar_wait_drain(bar(B_KFULL + s), (last / NK) & 1);
           }
-        }
+        for (int s = 0; s < NV; ++s)
+          if (v_it > uint32_t(s)) {
+            const uint32_t last = v_it - 1 - ((v_it - 1 - s) % NV);
+            mbar_wait_drain(bar(B_VFULL + s), (last / NV) & 1);
+          }
         if (qi > 0) mbar_wait_drain(bar(B_QFULL), (qi - 1) & 1);
       }
     }
@@ -200,33 +212,37 @@ __global__ void __launch_bounds__(384, 1)
         if (nt == 0) continue;
         if (!(ok = mbar_wait(bar(B_QFULL), qi & 1, abort_flag))) break;
         {
-          const int st0 = kv_it % NST;
-          if (!(ok = mbar_wait(bar(B_KFULL + st0), (kv_it / NST) & 1, abort_flag))) break;
+          const int sk0 = kv_it % NK;
+          if (!(ok = mbar_wait(bar(B_KFULL + sk0), (kv_it / NK) & 1, abort_flag))) break;
           tc_fence_after();
-          issue_s(0, st0);
+          issue_s(0, sk0);
           tc_commit(bar(B_SFULL + 0));
           if (slots == 2) {
-            issue_s(1, st0);
+            issue_s(1, sk0);
             tc_commit(bar(B_SFULL + 1));
           }
+          tc_commit(bar(B_KEMPTY + sk0));
           if (nt == 1) tc_commit(bar(B_QEMPTY));
         }
         for (int j = 1; j <= nt && ok; ++j) {
           const uint32_t itp = kv_it + j - 1, itn = kv_it + j;
-          const int sp = itp % NST, sn = itn % NST;
+          const int svp = itp % NV, skn = itn % NK;
           const uint32_t tp = tcount + j - 1;
-          if (j < nt && !(ok = mbar_wait(bar(B_KFULL + sn), (itn / NST) & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(bar(B_VFULL + sp), (itp / NST) & 1, abort_flag))) break;
+          if (j < nt && !(ok = mbar_wait(bar(B_KFULL + skn), (itn / NK) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(B_VFULL + svp), (itp / NV) & 1, abort_flag))) break;
           for (int s = 0; s < slots; ++s) {
             if (!(ok = mbar_wait(bar(B_PFULL + s), tp & 1, abort_flag))) break;
             if (j == 1 && !(ok = mbar_wait(bar(B_OEMPTY + s), (qi & 1) ^ 1, abort_flag))) break;
             tc_fence_after();
-            issue_pv(s, sp, j > 1);
-            if (s == slots - 1) tc_commit(bar(B_KVEMPTY + sp));
+            issue_pv(s, svp, j > 1);
+            if (s == slots - 1) tc_commit(bar(B_VEMPTY + svp));
             if (j < nt) {
-              issue_s(s, sn);
+              issue_s(s, skn);
               tc_commit(bar(B_SFULL + s));
-              if (s == slots - 1 && j == nt - 1) tc_commit(bar(B_QEMPTY));
+              if (s == slots - 1) {
+                tc_commit(bar(B_KEMPTY + skn));
+                if (j == nt - 1) tc_commit(bar(B_QEMPTY));
+              }
             } else {
               tc_commit(bar(B_OFINAL + s));
             }

@@ -15,6 +15,7 @@
 #include "bwd_aux.h"
 #include "host_util.h"
 #include "plan_layout.h"
+#include "ptx.cuh"
 
 namespace bd {
 
@@ -136,9 +137,37 @@ __global__ void __launch_bounds__(256) bd_owner_sum_kernel(OwnerSumArgs a) {
   *pv = ov;
 }
 
+// Waits, with the kernels' bounded wait, on an mbarrier that nothing arrives at,
+// then records the timeout in the plan's status word like any kernel would.
+__global__ void bd_selftest_wait_kernel(int32_t* plan, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t mbar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    dev::mbar_init(dev::smem_u32(&mbar), 1);
+    abort_flag = 0;
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = dev::mbar_wait(dev::smem_u32(&mbar), 0, &abort_flag, limit_ns);
+  if (!ok && threadIdx.x == 0) {
+    atomicExch(plan + H_STATUS, DEV_TIMEOUT);
+    atomicExch(plan + H_STATUS_DETAIL, 99);
+  }
+}
+
 }  // namespace bd
 
 using namespace bd;
+
+extern "C" int32_t bd_selftest_bounded_wait(const void* plan_dev, uint32_t limit_us, void* stream) {
+  if (!plan_dev || reinterpret_cast<uintptr_t>(plan_dev) % 16) return fail(BD_ERR_ARG, "plan_dev NULL/misaligned");
+  if (limit_us == 0 || limit_us > 1000000) return fail(BD_ERR_ARG, "limit_us must be in (0, 1e6]");
+  bd_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      const_cast<int32_t*>(static_cast<const int32_t*>(plan_dev)), uint64_t(limit_us) * 1000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bd_selftest_wait_kernel launch");
+  return ok();
+}
 
 extern "C" int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
                                 const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream) {

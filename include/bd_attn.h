@@ -241,6 +241,14 @@ BD_API size_t bd_attn_bwd_noalloc_capacity(void);
  * reset != 0 clears the status afterwards. */
 BD_API int32_t bd_check_status(const void* plan_dev, int32_t reset, void* stream);
 
+/* bd_selftest_bounded_wait -- failure-detection self test: launches a one-warp
+ * kernel that waits, with the same bounded wait every kernel of the library
+ * uses, on an mbarrier nothing arrives at; after limit_us microseconds
+ * (1..1e6) the wait gives up and the kernel records BD_ERR_DEVICE_TIMEOUT in
+ * the plan's status word, which bd_check_status then reports. Nothing faults
+ * and the context stays usable. */
+BD_API int32_t bd_selftest_bounded_wait(const void* plan_dev, uint32_t limit_us, void* stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 BD_API const char* bd_last_error(void);
 
