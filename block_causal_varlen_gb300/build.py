@@ -54,19 +54,22 @@ def _digest(extra=()) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, defines=()) -> str:
-    """Compile and link libbd.so if any source changed; returns its path."""
+def build(force: bool = False, verbose: bool = False, defines=(), out: str = LIB) -> str:
+    """Compile and link the library (default: libbd.so in the package) if any
+    source changed; returns its path. ``defines`` adds -D flags (e.g. BD_TRACE
+    for the tracing build, which should go to another ``out`` path)."""
     defs = [f"-D{d}" for d in defines]
-    stamp = os.path.join(BUILD, "stamp")
+    build_dir = BUILD if out == LIB else out + ".build"
+    stamp = os.path.join(build_dir, "stamp")
     dig = _digest(defs)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == dig:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and os.path.exists(out) and os.path.exists(stamp) and open(stamp).read() == dig:
+        return out
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *NVFLAGS, *defs, "-I", INCLUDE, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -80,15 +83,15 @@ def build(force: bool = False, verbose: bool = False, defines=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     with open(stamp, "w") as fh:
         fh.write(dig)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":

@@ -231,13 +231,16 @@ __global__ void __launch_bounds__(384, 1)
           if (j < nt && !(ok = mbar_wait(bar(B_KFULL + skn), (itn / NK) & 1, abort_flag))) break;
           if (!(ok = mbar_wait(bar(B_VFULL + svp), (itp / NV) & 1, abort_flag))) break;
           for (int s = 0; s < slots; ++s) {
+            BD_TRACE_EVENT(14 + s, int(tp));  // MMA: starts waiting for P
             if (!(ok = mbar_wait(bar(B_PFULL + s), tp & 1, abort_flag))) break;
             if (j == 1 && !(ok = mbar_wait(bar(B_OEMPTY + s), (qi & 1) ^ 1, abort_flag))) break;
             tc_fence_after();
+            BD_TRACE_EVENT(10 + s, int(tp));  // MMA: P ready, PV issued
             issue_pv(s, svp, j > 1);
             if (s == slots - 1) tc_commit(bar(B_VEMPTY + svp));
             if (j < nt) {
               issue_s(s, skn);
+              BD_TRACE_EVENT(12 + s, int(tcount + j));  // MMA: S issued
               tc_commit(bar(B_SFULL + s));
               if (s == slots - 1) {
                 tc_commit(bar(B_KEMPTY + skn));
@@ -295,8 +298,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         float m_run = -CUDART_INF_F, l_run = 0.f;
         for (int j = 0; j < nt; ++j, ++tcount) {
+          if (r == 0) BD_TRACE_EVENT(20 + s, int(tcount));  // softmax: start waiting for S
           if (!(ok = mbar_wait(bar(B_SFULL + s), tcount & 1, abort_flag))) break;
           tc_fence_after();
+          if (r == 0) BD_TRACE_EVENT(30 + s, int(tcount));  // softmax: S ready
           uint32_t u[4][32];
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, u[q]);
@@ -326,6 +331,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], x[e + k], x[e + 8 + k]);
           const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+          if (r == 0) BD_TRACE_EVENT(40 + s, int(tcount));  // softmax: row max done
           const float m_new = fmaxf(m_run, mx * a.scale_log2);
           const bool need = m_new > m_run + 8.0f;
           float factor = 1.f;
@@ -365,11 +371,14 @@ __global__ void __launch_bounds__(384, 1)
           const float2 st = fadd2(s01, s23);
           const float sum = st.x + st.y;
           l_run += sum;
+          if (r == 0) BD_TRACE_EVENT(50 + s, int(tcount));  // softmax: exponentials done
           tmem_st32(tS, pk[0]);
           tmem_st32(tS + 32, pk[1]);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(B_PFULL + s));
+          if (r == 0) BD_TRACE_EVENT(60 + s, int(tcount));  // softmax: P stored
+          if (lane == 0) BD_TRACE_EVENT(40 + 8 + 4 * s + quarter, int(tcount));  // per warp: P stored
         }
         if (!ok) break;
         if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
@@ -439,6 +448,21 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
 }  // namespace bd
 
 using namespace bd;
+
+#ifdef BD_TRACE
+// Trace build only: copies the [site][tile] clock table of CTA 0 to host memory
+// (cap entries) and clears it; returns the number of entries copied.
+extern "C" BD_API int32_t bd_trace_read(unsigned long long* host, int32_t cap) {
+  const int32_t n = dev::kTraceSites * dev::kTraceTiles;
+  const int32_t k = n < cap ? n : cap;
+  cudaDeviceSynchronize();
+  if (k > 0) cudaMemcpyFromSymbol(host, dev::g_bd_trace, size_t(k) * 8);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, dev::g_bd_trace) == cudaSuccess) cudaMemset(p, 0, size_t(n) * 8);
+  cudaDeviceSynchronize();
+  return k;
+}
+#endif
 
 extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
                                const bd_tensor* v, int32_t row_offset, bd_tensor* out, bd_rowstat* lse,

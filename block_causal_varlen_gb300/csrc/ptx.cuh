@@ -48,20 +48,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware park the thread until the phase completes
+// (or kSuspendNs passes) instead of returning at once, so waiting warps do not
+// take issue slots from the warps doing the work.
+constexpr uint32_t kSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity. Returns false (and sets
 // *abort) after limit_ns of global time, or as soon as another role has set *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
     }
   }
 }
@@ -70,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // flag so that copies and MMAs already in flight are still waited for.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_suspend(bar, parity))
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   return true;
 }
@@ -340,6 +354,24 @@ __device__ __forceinline__ bool elect_one() {
       : "=r"(pred));
   return pred != 0;
 }
+
+// ---------------------------------------------------------------- tracing
+// Built with -DBD_TRACE, kernels record (site, tile, clock64) events of CTA 0
+// into a device array for timeline analysis; without it the macro is empty.
+#ifdef BD_TRACE
+constexpr int kTraceSites = 64, kTraceTiles = 1024;
+// one buffer per translation unit (the forward kernel's file reads its own back);
+// slot [site][tile] holds clock64() of CTA 0: plain stores, no atomics, so that
+// recording does not stall the recording warp
+static __device__ unsigned long long g_bd_trace[kTraceSites * kTraceTiles];
+__device__ __forceinline__ void trace_event(int site, int tile) {
+  if (blockIdx.x != 0 || tile < 0 || tile >= kTraceTiles || site < 0 || site >= kTraceSites) return;
+  g_bd_trace[site * kTraceTiles + tile] = clock64();
+}
+#define BD_TRACE_EVENT(site, tile) ::bd::dev::trace_event((site), (tile))
+#else
+#define BD_TRACE_EVENT(site, tile) ((void)0)
+#endif
 
 }  // namespace dev
 }  // namespace bd
