@@ -25,7 +25,7 @@ from . import _abi
 from ._abi import (BD_KV_GATHER, BD_KV_WINDOW, BDError, bd_chunk_hdr, bd_rowstat, bd_segment_t,  # noqa: F401
                    bd_tensor, check, load)
 
-__all__ = ["Plan", "bd_segment", "bd_attn_fwd", "bd_attn_bwd", "bd_attn_bwd_pre", "bd_attn_bwd_main",
+__all__ = ["Plan", "bd_segment", "bd_doc_ids_to_cu", "bd_exchange_plan", "bd_attn_fwd", "bd_attn_bwd", "bd_attn_bwd_pre", "bd_attn_bwd_main",
            "bd_owner_sum", "bd_check_status",
            "bd_attn_bwd_workspace", "attn_fwd", "attn_bwd", "BD_KV_GATHER", "BD_KV_WINDOW", "BDError", "load"]
 
@@ -48,6 +48,30 @@ def bd_segment(cu_seqlens, S: int, cp: int, rank: int):
     check(lib.bd_segment(pcu, len(cu) - 1, S, cp, rank, C.byref(hdr), segs, hdr.nseg))
     return ({f: getattr(hdr, f) for f in _HDR_FIELDS},
             [tuple(getattr(segs[i], f) for f in _SEG_FIELDS) for i in range(hdr.nseg)])
+
+
+def bd_doc_ids_to_cu(doc_ids):
+    """cu_seqlens (list) from a 1-D per-token document-id array (negative = padding suffix)."""
+    lib = load()
+    ids, pids = _i32(doc_ids)
+    nd = C.c_int32()
+    st = lib.bd_doc_ids_to_cu(pids, len(ids), None, 0, C.byref(nd))
+    if st not in (0, _abi.BD_ERR_CAPACITY):
+        check(st)
+    out = (C.c_int32 * (nd.value + 1))()
+    check(lib.bd_doc_ids_to_cu(pids, len(ids), out, nd.value + 1, C.byref(nd)))
+    return list(out)
+
+
+def bd_exchange_plan(cu_seqlens, S: int, cp: int, rank: int):
+    """Needed-only K/V exchange of chunk ``rank``: (kind, [(src_rank, src_row, n_rows, dst_row), ...])."""
+    lib = load()
+    cu, pcu = _i32(cu_seqlens)
+    kind, n = C.c_int32(), C.c_int32()
+    check(lib.bd_exchange_plan(pcu, len(cu) - 1, S, cp, rank, C.byref(kind), None, 0, C.byref(n)))
+    xs = (_abi.bd_xfer_t * max(1, n.value))()
+    check(lib.bd_exchange_plan(pcu, len(cu) - 1, S, cp, rank, C.byref(kind), xs, n.value, C.byref(n)))
+    return kind.value, [(x.src_rank, x.src_row, x.n_rows, x.dst_row) for x in xs[:n.value]]
 
 
 class Plan:

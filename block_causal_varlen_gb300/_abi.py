@@ -37,6 +37,13 @@ class bd_chunk_hdr(C.Structure):
                                           "kv_start", "kv_end", "nseg")]
 
 
+class bd_xfer_t(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("src_rank", "src_row", "n_rows", "dst_row")]
+
+
+BD_XCHG_LOCAL, BD_XCHG_HALO, BD_XCHG_A2A = 0, 1, 2
+
+
 class bd_plan_desc(C.Structure):
     _fields_ = [("B", C.c_int32), ("S", C.c_int32), ("cp", C.c_int32), ("nchunks", C.c_int32),
                 ("ranks", C.POINTER(C.c_int32)), ("H", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32),
@@ -59,6 +66,11 @@ EXPORTS = {
     "bd_segment": (C.c_int32, [C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                C.POINTER(bd_chunk_hdr), C.POINTER(bd_segment_t), C.c_int32]),
     "bd_padded_len": (C.c_int32, [C.c_int32, C.c_int32]),
+    "bd_doc_ids_to_cu": (C.c_int32, [C.POINTER(C.c_int32), C.c_int32, C.POINTER(C.c_int32), C.c_int32,
+                                     C.POINTER(C.c_int32)]),
+    "bd_exchange_plan": (C.c_int32, [C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                     C.POINTER(C.c_int32), C.POINTER(bd_xfer_t), C.c_int32,
+                                     C.POINTER(C.c_int32)]),
     "bd_plan_bytes": (C.c_int32, [C.POINTER(bd_plan_desc), C.POINTER(C.c_size_t)]),
     "bd_plan_build": (C.c_int32, [C.POINTER(bd_plan_desc), C.c_void_p, C.c_size_t]),
     "bd_plan_chunk": (C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(bd_chunk_hdr), C.POINTER(bd_segment_t),

@@ -130,6 +130,56 @@ extern "C" int32_t bd_segment(const int32_t* cu, int32_t ndocs, int32_t S, int32
   return ok();
 }
 
+extern "C" int32_t bd_doc_ids_to_cu(const int32_t* ids, int32_t n, int32_t* cu_out, int32_t cap,
+                                    int32_t* ndocs_out) {
+  if (!ids || !ndocs_out || n < 0) return fail(BD_ERR_ARG, "doc_ids / ndocs_out NULL or n < 0");
+  int32_t valid = 0;
+  while (valid < n && ids[valid] >= 0) ++valid;
+  for (int32_t t = valid; t < n; ++t)
+    if (ids[t] >= 0) return fail(BD_ERR_CU_SEQLENS, "padding (negative id) at %d is not a suffix", valid);
+  int32_t nd = 0;
+  for (int32_t t = 0; t < valid; ++t) {
+    if (t > 0 && ids[t] < ids[t - 1])
+      return fail(BD_ERR_CU_SEQLENS, "document ids decrease at token %d (%d -> %d)", t, ids[t - 1], ids[t]);
+    if (t == 0 || ids[t] != ids[t - 1]) ++nd;
+  }
+  *ndocs_out = nd;
+  if (!cu_out || cap < nd + 1) return fail(BD_ERR_CAPACITY, "cu_out needs %d entries", nd + 1);
+  int32_t k = 0;
+  cu_out[k++] = 0;
+  for (int32_t t = 1; t <= valid; ++t)
+    if (t == valid || ids[t] != ids[t - 1]) cu_out[k++] = t;
+  if (valid == 0) k = 1;
+  return ok();
+}
+
+extern "C" int32_t bd_exchange_plan(const int32_t* cu, int32_t ndocs, int32_t S, int32_t cp, int32_t rank,
+                                    int32_t* kind_out, bd_xfer_t* xfers, int32_t cap, int32_t* nxfer_out) {
+  if (!kind_out || !nxfer_out) return fail(BD_ERR_ARG, "kind_out / nxfer_out NULL");
+  bd_chunk_hdr h;
+  int32_t st = bd_segment(cu, ndocs, S, cp, rank, &h, nullptr, 0);
+  if (st) return st;
+  const int32_t L = h.L;
+  int32_t n = 0, remote_owners = 0;
+  if (h.kv_end > h.kv_start) {
+    for (int32_t o = h.kv_start / L; o <= (h.kv_end - 1) / L; ++o) {
+      const int32_t lo = std::max(h.kv_start, o * L), hi = std::min(h.kv_end, (o + 1) * L);
+      if (hi <= lo) continue;
+      if (xfers && n < cap) {
+        xfers[n].src_rank = o; xfers[n].src_row = lo; xfers[n].n_rows = hi - lo;
+        xfers[n].dst_row = lo - h.kv_start;
+      }
+      ++n;
+      if (o != rank) ++remote_owners;
+    }
+  }
+  *nxfer_out = n;
+  *kind_out = remote_owners == 0 ? BD_XCHG_LOCAL
+              : (remote_owners == 1 && h.kv_start >= (rank - 1) * L) ? BD_XCHG_HALO : BD_XCHG_A2A;
+  if (xfers && n > cap) return fail(BD_ERR_CAPACITY, "exchange needs %d transfers, capacity %d", n, cap);
+  return ok();
+}
+
 namespace {
 
 struct Built {

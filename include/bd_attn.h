@@ -109,6 +109,43 @@ BD_API int32_t bd_segment(const int32_t* cu_seqlens, int32_t ndocs, int32_t S, i
 /* Smallest multiple of cp that is >= s (the padding step of batch.py). */
 BD_API int32_t bd_padded_len(int32_t s, int32_t cp);
 
+/* bd_doc_ids_to_cu -- cu_seqlens from a 1-D per-token document-id array (the
+ * page's "1-D document ids" input, NeMo Automodel page "block-diagonal varlen
+ * CP for packed sequences", Proof). doc_ids: host int32[n]; a document is a
+ * maximal run of equal ids; ids must be non-decreasing over the valid tokens;
+ * negative ids mark padding and may only form a suffix. Writes ndocs+1 entries
+ * to cu_out (cap entries available) and ndocs to *ndocs_out.
+ * Errors: BD_ERR_ARG, BD_ERR_CU_SEQLENS (decreasing ids, padding not a
+ * suffix), BD_ERR_CAPACITY (cap too small; *ndocs_out still set). */
+BD_API int32_t bd_doc_ids_to_cu(const int32_t* doc_ids, int32_t n, int32_t* cu_out, int32_t cap,
+                         int32_t* ndocs_out);
+
+/* One transfer of a needed-only K/V exchange: global rows
+ * [src_row, src_row + n_rows) owned by rank src_rank land at row dst_row of
+ * the receiving rank's window buffer. In the backward the same rows of the
+ * window's dK/dV go back to src_rank and are added at src_row (index_add). */
+typedef struct {
+  int32_t src_rank, src_row, n_rows, dst_row;
+} bd_xfer_t;
+
+typedef enum {
+  BD_XCHG_LOCAL = 0, /* the window lies inside the rank's own rows (or is empty) */
+  BD_XCHG_HALO = 1,  /* remote rows come from the left neighbour only          */
+  BD_XCHG_A2A = 2    /* remote rows come from two or more ranks (all-to-all-v) */
+} bd_xchg_kind;
+
+/* bd_exchange_plan -- the transfers that build rank `rank`'s needed-only K/V
+ * window [kv_start, kv_end) from the contiguous owner slices (rank q owns rows
+ * [q*L, (q+1)*L)): left-neighbour halo when a straddling document reaches back
+ * one rank, all-to-all-v when it reaches further (same page, Summary; Design
+ * overview, exchange.py). Transfers are in increasing src_rank order and cover
+ * the window exactly once; the rank's own rows appear as a transfer from
+ * itself. xfers may be NULL to count only. Errors as bd_segment, plus
+ * BD_ERR_CAPACITY. */
+BD_API int32_t bd_exchange_plan(const int32_t* cu_seqlens, int32_t ndocs, int32_t S, int32_t cp,
+                         int32_t rank, int32_t* kind_out, bd_xfer_t* xfers, int32_t cap,
+                         int32_t* nxfer_out);
+
 /* Description of a step's work: B packed sequences of padded length S, each cut
  * into cp chunks of L = S/cp rows, of which the plan covers `nchunks` (chunk c
  * of the plan is rank ranks[c]; ranks == NULL means ranks 0..nchunks-1). One

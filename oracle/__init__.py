@@ -29,6 +29,7 @@ pieces are pinned by ``tests/test_oracle.py`` and ``tests/test_segment.py``
 against brute force, library special cases, closed forms and invariants.
 """
 from .segment import doc_ids, segment_chunk, useful_pairs  # noqa: F401
+from .exchange import doc_ids_to_cu, exchange_plan  # noqa: F401
 from .attention import (  # noqa: F401
     block_causal_mask, attention_fwd, attention_bwd, chunk_fwd, chunk_bwd,
     attention_bwd_cols, attention_bwd_rows,
