@@ -119,6 +119,28 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+KERNEL_SOURCES = {"bd_fwd_kernel": "attn_fwd.cu", "bd_bwd_kernel": "attn_bwd.cu"}
+
+
+def kernel_traffic(kernel, workload):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from the ncu
+    capture recorded in profiles/traffic.json, or None when there is none or the
+    kernel's source changed since the counters were taken."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(prof) or kernel not in KERNEL_SOURCES:
+        return None
+    try:
+        rec = json.load(open(prof)).get(f"{kernel}:{workload}")
+        src = os.path.join(ROOT, "block_causal_varlen_gb300", "csrc", KERNEL_SOURCES[kernel])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec and rec.get("source_sha256") == digest:
+            return rec.get("bytes")
+    except Exception:
+        pass
+    return None
+
+
 def useful_flops(plan, wl):
     n = plan.useful_pairs() * wl.H
     return n, 4.0 * wl.d * n, 10.0 * wl.d * n
@@ -373,13 +395,7 @@ def run_ours(args):
     dom_ms = t_main if dominant == "bd_bwd_kernel" else t_fwd
     dom_flops = f_bwd if dominant == "bd_bwd_kernel" else f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get(f"{dominant}:{wl.name}")
-        except Exception:
-            traffic = None
+    traffic = kernel_traffic(dominant, wl.name)
 
     result = None
     if rank == 0:

@@ -224,15 +224,20 @@ __global__ void __launch_bounds__(512, 1)
         for (int s = 0; s < nsteps && ok; ++s, ++sc) {
           const int qs = sc & 1;
           const uint32_t sQs = sQ + qs * Cfg::kTileBytes;
+          BD_TRACE_EVENT(0, int(sc));  // MMA: step start (waits dO, dQ drained)
           if (!(ok = mbar_wait(bar(C_DOFULL), sc & 1, abort_flag))) break;
+          BD_TRACE_EVENT(1, int(sc));
           if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
+          BD_TRACE_EVENT(2, int(sc));  // MMA: dP^T issue
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + Cfg::kColDP, kmaj(sV, kk), kmaj(sDO, kk), idSS, kk > 0);
           tc_commit(bar(C_DPFULL));
+          BD_TRACE_EVENT(3, int(sc));  // MMA: waits P
           if (!(ok = mbar_wait(bar(C_PREADY), sc & 1, abort_flag))) break;
           if (s == 0 && !(ok = mbar_wait(bar(C_ACCEMPTY), (u & 1) ^ 1, abort_flag))) break;
+          BD_TRACE_EVENT(4, int(sc));  // MMA: dV issue
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -247,7 +252,9 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             issue_s(sc + 1);
           }
+          BD_TRACE_EVENT(5, int(sc));  // MMA: waits dS
           if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
+          BD_TRACE_EVENT(6, int(sc));  // MMA: dQ/dK issue
           tc_fence_after();
           // dQ first: its drain gates the next step's dP^T (same TMEM columns)
 #pragma unroll
@@ -257,6 +264,7 @@ __global__ void __launch_bounds__(512, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + Cfg::kColDK, kmaj(sDS, kk), mnmaj(sQs, kk), idKM, (s > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(C_QEMPTY0 + qs));  // Q and dS^T of this step are free after dK
+          BD_TRACE_EVENT(7, int(sc));  // MMA: dK issued
           if (s == nsteps - 1) {
             tc_commit(bar(C_ACCDONE));
             tc_commit(bar(C_KVEMPTY));
@@ -295,7 +303,9 @@ __global__ void __launch_bounds__(512, 1)
             const float* st_d = st_lse + 128;
             const int32_t* st_ds = reinterpret_cast<const int32_t*>(st_lse + 256);
             if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
+            if (threadIdx.x == 128) BD_TRACE_EVENT(10, int(sc));  // compute: waits S
             if (!(ok = mbar_wait(bar(C_SFULL), sc & 1, abort_flag))) break;
+            if (threadIdx.x == 128) BD_TRACE_EVENT(11, int(sc));  // compute: S ready
             tc_fence_after();
             // Rows' document starts are non-decreasing and invalid rows carry
             // INT_MAX, so key j sees every query of the tile iff it lies at or
@@ -334,7 +344,9 @@ __global__ void __launch_bounds__(512, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(C_PREADY));
+            if (threadIdx.x == 128) BD_TRACE_EVENT(12, int(sc));  // compute: P stored
             if (!(ok = mbar_wait(bar(C_DPFULL), sc & 1, abort_flag))) break;
+            if (threadIdx.x == 128) BD_TRACE_EVENT(13, int(sc));  // compute: dP ready
             tc_fence_after();
             // dS^T of the previous step must have been consumed by its dQ and dK MMAs
             // (dK is the later one; its commit also releases that step's Q stage)
@@ -370,6 +382,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(C_DSREADY));
+            if (threadIdx.x == 128) BD_TRACE_EVENT(14, int(sc));  // compute: dS stored
           }
       }
     }
@@ -411,7 +424,9 @@ __global__ void __launch_bounds__(512, 1)
             const int lrow = t * 128 + rl;
             const bool qrow_ok = lrow < a.L && r0 + lrow < svalid;
             // the warpgroup meets at named barriers below: leave together or not at all
+            if (rl == 0) BD_TRACE_EVENT(20, int(sc));  // dQ: waits dQ
             ok = bar_red_and(1, 128, mbar_wait(bar(C_DQFULL), sc & 1, abort_flag));
+            if (rl == 0) BD_TRACE_EVENT(21, int(sc));  // dQ: dQ ready
             if (!ok) break;
             tc_fence_after();
             // dQ tile (128 query rows x D fp32) goes to global memory as D/32
@@ -426,6 +441,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int q = 0; q < D / 32; ++q) reg_fence(r[q]);
             tc_fence_before();
             mbar_arrive(bar(C_DQEMPTY));
+            if (rl == 0) BD_TRACE_EVENT(22, int(sc));  // dQ: TMEM released
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
               if (rl == 0) bulk_wait_read<0>();  // the previous box has left the staging tile
@@ -527,6 +543,20 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
 }  // namespace bd
 
 using namespace bd;
+
+#ifdef BD_TRACE
+// Trace build only: the backward kernel's [site][tile] clock table of CTA 0.
+extern "C" BD_API int32_t bd_trace_read_bwd(unsigned long long* host, int32_t cap) {
+  const int32_t n = dev::kTraceSites * dev::kTraceTiles;
+  const int32_t k = n < cap ? n : cap;
+  cudaDeviceSynchronize();
+  if (k > 0) cudaMemcpyFromSymbol(host, dev::g_bd_trace, size_t(k) * 8);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, dev::g_bd_trace) == cudaSuccess) cudaMemset(p, 0, size_t(n) * 8);
+  cudaDeviceSynchronize();
+  return k;
+}
+#endif
 
 extern "C" int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes) {
   PlanView pv;
