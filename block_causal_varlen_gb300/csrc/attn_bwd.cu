@@ -71,7 +71,7 @@ struct BwdCfg {
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
-  static constexpr int kRegsCtl = 88, kRegsCompute = 128, kRegsDq = 168;
+  static constexpr int kRegsCtl = 96, kRegsCompute = 120, kRegsDq = 176;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
   static constexpr int kRegsLaunch = 128;  // 65536 / 512 threads: what ptxas assigns at launch
   static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
@@ -203,8 +203,15 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idKM = idesc_bf16(128, D, false, true);   // A K-major, B MN-major
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);    // both MN-major
-      auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024); };
-      auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); };
+      // base descriptors of every operand tile are built once; a K step only
+      // advances the start-address field (16-byte units) with a 64-bit add
+      const uint32_t dK_k = sdesc_lo(sK, 16), dV_k = sdesc_lo(sV, 16), dK_mn = sdesc_lo(sK, 16384);
+      const uint32_t dDO_k = sdesc_lo(sDO, 16), dDO_mn = sdesc_lo(sDO, 16384);
+      const uint32_t dDS_k = sdesc_lo(sDS, 16), dDS_mn = sdesc_lo(sDS, 16384);
+      auto dQ_k = [&](int qs) { return sdesc_lo(sQ + qs * Cfg::kTileBytes, 16); };
+      auto dQ_mn = [&](int qs) { return sdesc_lo(sQ + qs * Cfg::kTileBytes, 16384); };
+      auto kstep = [](int kk) { return uint32_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+      auto mnstep = [](int kk) { return uint32_t((kk * 2048) >> 4); };
       uint32_t u = 0, sc = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
@@ -213,9 +220,9 @@ __global__ void __launch_bounds__(512, 1)
         if (nsteps == 0) continue;
         if (!(ok = mbar_wait(bar(C_KVFULL), u & 1, abort_flag))) break;
         auto issue_s = [&](uint32_t step) {  // S^T = K Q^T for the Q tile of `step`
-          const uint32_t sQs = sQ + (step & 1) * Cfg::kTileBytes;
+          const uint32_t qd = dQ_k(step & 1);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmaj(sK, kk), kmaj(sQs, kk), idSS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss_lo(tmem, dK_k + kstep(kk), qd + kstep(kk), idSS, kk > 0);
           tc_commit(bar(C_SFULL));
         };
         if (!(ok = mbar_wait(bar(C_QFULL0 + (sc & 1)), (sc >> 1) & 1, abort_flag))) break;
@@ -223,7 +230,6 @@ __global__ void __launch_bounds__(512, 1)
         issue_s(sc);
         for (int s = 0; s < nsteps && ok; ++s, ++sc) {
           const int qs = sc & 1;
-          const uint32_t sQs = sQ + qs * Cfg::kTileBytes;
           BD_TRACE_EVENT(0, int(sc));  // MMA: step start (waits dO, dQ drained)
           if (!(ok = mbar_wait(bar(C_DOFULL), sc & 1, abort_flag))) break;
           BD_TRACE_EVENT(1, int(sc));
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, kmaj(sV, kk), kmaj(sDO, kk), idSS, kk > 0);
+            mma_ss_lo(tmem + Cfg::kColDP, dV_k + kstep(kk), dDO_k + kstep(kk), idSS, kk > 0);
           tc_commit(bar(C_DPFULL));
           BD_TRACE_EVENT(3, int(sc));  // MMA: waits P
           if (!(ok = mbar_wait(bar(C_PREADY), sc & 1, abort_flag))) break;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + Cfg::kColDV, tmem + (kk >> 2) * 64 + (kk & 3) * 8, mnmaj(sDO, kk), idKM,
+            mma_ts_lo(tmem + Cfg::kColDV, tmem + (kk >> 2) * 64 + (kk & 3) * 8, dDO_mn + mnstep(kk), idKM,
                    (s > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(C_DOEMPTY));
           // the next step's scores go ahead of this step's dK / dQ so that the
@@ -258,11 +264,12 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           // dQ first: its drain gates the next step's dP^T (same TMEM columns)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + Cfg::kColDP, mnmaj(sDS, kk), mnmaj(sK, kk), idMM, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss_lo(tmem + Cfg::kColDP, dDS_mn + mnstep(kk), dK_mn + mnstep(kk), idMM, kk > 0);
           tc_commit(bar(C_DQFULL));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + Cfg::kColDK, kmaj(sDS, kk), mnmaj(sQs, kk), idKM, (s > 0 || kk > 0) ? 1u : 0u);
+            mma_ss_lo(tmem + Cfg::kColDK, dDS_k + kstep(kk), dQ_mn(qs) + mnstep(kk), idKM, (s > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(C_QEMPTY0 + qs));  // Q and dS^T of this step are free after dK
           BD_TRACE_EVENT(7, int(sc));  // MMA: dK issued
           if (s == nsteps - 1) {
@@ -422,7 +429,6 @@ __global__ void __launch_bounds__(512, 1)
           for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
             const int h = g * a.G + hh;
             const int lrow = t * 128 + rl;
-            const bool qrow_ok = lrow < a.L && r0 + lrow < svalid;
             // the warpgroup meets at named barriers below: leave together or not at all
             if (rl == 0) BD_TRACE_EVENT(20, int(sc));  // dQ: waits dQ
             ok = bar_red_and(1, 128, mbar_wait(bar(C_DQFULL), sc & 1, abort_flag));

@@ -188,22 +188,23 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      // descriptors are built once per operand tile; a K step only advances the
+      // start-address field (16-byte units) with a 64-bit add
       auto issue_s = [&](int s, int st) {
         const uint32_t d_t = tmem + s * 128;
+        const uint32_t qa = sdesc_lo(sQ + s * Cfg::kTileBytes, 16), kb = sdesc_lo(sK + st * Cfg::kTileBytes, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(d_t, sdesc_sw128(sQ + s * Cfg::kTileBytes + off, 16, 1024),
-                 sdesc_sw128(sK + st * Cfg::kTileBytes + off, 16, 1024), idS, kk > 0);
+          const uint32_t off = uint32_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_ss_lo(d_t, qa + off, kb + off, idS, kk > 0);
         }
       };
       auto issue_pv = [&](int s, int st, bool acc) {
         const uint32_t d_t = tmem + Cfg::kOCol + s * D;
         const uint32_t p_t = tmem + s * 128;
+        const uint32_t vb = sdesc_lo(sV + st * Cfg::kTileBytes, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(d_t, p_t + kk * 8, sdesc_sw128(sV + st * Cfg::kTileBytes + kk * 2048, 16384, 1024), idPV,
-                 (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) mma_ts_lo(d_t, p_t + kk * 8, vb + uint32_t(kk * 128), idPV, (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t kv_it = 0, qi = 0, tcount = 0;
       bool ok = true;
