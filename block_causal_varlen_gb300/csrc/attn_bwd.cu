@@ -24,8 +24,8 @@
 //   warps 4-11   P^T and dS^T for the tile's 128 keys (lane = key row), two
 //                warps per lane quarter, one per 64-query half.
 //   warps 12-15  read dQ out of TMEM and add it into global memory with TMA
-//                reduce-adds (128 x 32 fp32 boxes staged in shared memory); at
-//                the end of a unit write dK (x scale) and dV.
+//                reduce-adds (128 x 16 fp32 boxes staged through two shared
+//                memory buffers); at the end of a unit write dK (x scale) and dV.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV, dK after that.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -65,7 +65,7 @@ struct BwdCfg {
   static constexpr int kOffDS = 5 * kTileBytes;         // dS^T, 128 keys x 128 queries bf16
   static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128], ds[128]
   static constexpr int kStatBytes = 3 * 512;
-  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;  // dQ staging, 128 rows x 128 bytes
+  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;  // dQ staging, two 128 rows x 64 bytes buffers
   static constexpr int kOffBar = kOffStage + 16384;
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -161,33 +161,46 @@ __global__ void __launch_bounds__(512, 1)
         }
         ++u;
         const StepRange R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+        // Q / dO / row statistics of a step are loaded once its stage is free, which
+        // is late (the stage's previous Q is read by the last MMA of the step before);
+        // so each step's tiles are first prefetched into L2 one step ahead
+        struct Step { int it, t, h, b, c; };
+        Step prev{};
+        bool have_prev = false;
+        auto load_step = [&](const Step& x) {
+          const int qs = sc & 1;
+          if (!(ok = mbar_wait(bar(C_QEMPTY0 + qs), ((sc >> 1) & 1) ^ 1, abort_flag))) return;
+          mbar_expect_tx(bar(C_QFULL0 + qs), Cfg::kTileBytes + Cfg::kStatBytes);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_5d(sQ + qs * Cfg::kTileBytes + hf * 16384, &tm_q, bar(C_QFULL0 + qs), hf * 64, x.h, x.t * 128,
+                        x.c, x.b);
+          const uint32_t st = sbase + Cfg::kOffStat + qs * Cfg::kStatBytes;
+          const int64_t srow = (int64_t(x.it) * a.H + x.h) * a.Lpad + x.t * 128;
+          bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
+          bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
+          bulk_load(st + 1024, a.rowds + int64_t(x.it) * a.Lpad + x.t * 128, 512, bar(C_QFULL0 + qs));
+          ++q_iss;
+          if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) return;
+          mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_5d(sDO + hf * 16384, &tm_do, bar(C_DOFULL), hf * 64, x.h, x.t * 128, x.c, x.b);
+          ++do_iss;
+          ++sc;
+        };
         for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
           int t0, t1, r0;
           if (!R.tiles(it, t0, t1, r0)) continue;
           const int32_t* I = items + it * kItemWords;
           const int b = I[I_B], c = I[I_C];
           for (int t = t0; t <= t1 && ok; ++t)
-            for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
-              const int h = g * a.G + hh;
-              const int qs = sc & 1;
-              if (!(ok = mbar_wait(bar(C_QEMPTY0 + qs), ((sc >> 1) & 1) ^ 1, abort_flag))) break;
-              mbar_expect_tx(bar(C_QFULL0 + qs), Cfg::kTileBytes + Cfg::kStatBytes);
-              for (int hf = 0; hf < D / 64; ++hf)
-                tma_load_5d(sQ + qs * Cfg::kTileBytes + hf * 16384, &tm_q, bar(C_QFULL0 + qs), hf * 64, h, t * 128,
-                            c, b);
-              const uint32_t st = sbase + Cfg::kOffStat + qs * Cfg::kStatBytes;
-              const int64_t srow = (int64_t(it) * a.H + h) * a.Lpad + t * 128;
-              bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
-              bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
-              bulk_load(st + 1024, a.rowds + int64_t(it) * a.Lpad + t * 128, 512, bar(C_QFULL0 + qs));
-              ++q_iss;
-              if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) break;
-              mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
-              for (int hf = 0; hf < D / 64; ++hf)
-                tma_load_5d(sDO + hf * 16384, &tm_do, bar(C_DOFULL), hf * 64, h, t * 128, c, b);
-              ++do_iss;
+            for (int hh = 0; hh < a.G && ok; ++hh) {
+              const Step x{it, t, g * a.G + hh, b, c};
+              if (have_prev) load_step(prev);
+              prev = x;
+              have_prev = true;
             }
         }
+        if (have_prev && ok) load_step(prev);
       }
       if (!ok) {
         // wait for copies already issued before the shared memory goes away
@@ -252,7 +265,9 @@ __global__ void __launch_bounds__(512, 1)
           tc_commit(bar(C_DOEMPTY));
           // the next step's scores go ahead of this step's dK / dQ so that the
           // P^T warps can start on them while the tensor core finishes this step
-          // (P^T of this step, in the same TMEM columns, was read by dV above)
+          // (P^T of this step, in the same TMEM columns, was read by dV above);
+          // if its Q tile has not landed yet they go after dQ, else after dK, so
+          // that a late Q never holds up this step's own MMAs
           if (s + 1 < nsteps) {
             if (!(ok = mbar_wait(bar(C_QFULL0 + ((sc + 1) & 1)), ((sc + 1) >> 1) & 1, abort_flag))) break;
             tc_fence_after();
@@ -399,7 +414,6 @@ __global__ void __launch_bounds__(512, 1)
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // query row (dQ) or key row (dK/dV) == TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    const uint32_t stg_row = sStage + rl * 128;
     uint32_t u = 0, sc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
@@ -435,10 +449,9 @@ __global__ void __launch_bounds__(512, 1)
             if (rl == 0) BD_TRACE_EVENT(21, int(sc));  // dQ: dQ ready
             if (!ok) break;
             tc_fence_after();
-            // dQ tile (128 query rows x D fp32) goes to global memory as D/32
-            // reduce-adds of 128 x 32 boxes staged through shared memory in the
-            // 128-byte-swizzled layout (rows past L are clipped by the map).
-            // the whole dQ row leaves TMEM first, so the next dP^T can start at once
+            // dQ tile (128 query rows x D fp32) goes to global memory as TMA
+            // reduce-adds (rows past L are clipped by the map); the whole dQ row
+            // leaves TMEM first, so the next dP^T can start at once
             uint32_t r[D / 32][32];
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r[q]);
@@ -448,21 +461,26 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(bar(C_DQEMPTY));
             if (rl == 0) BD_TRACE_EVENT(22, int(sc));  // dQ: TMEM released
+            // D/16 rounds of 128 rows x 16 columns through two 8 KB staging buffers
+            // (64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)), so
+            // that filling one buffer overlaps the TMA reading the other
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-              if (rl == 0) bulk_wait_read<0>();  // the previous box has left the staging tile
+            for (int q = 0; q < D / 16; ++q) {
+              const uint32_t buf = sStage + (q & 1) * 8192;
+              if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
               named_bar_sync(1, 128);
+              const uint32_t* v = r[q >> 1] + (q & 1) * 16;
 #pragma unroll
-              for (int c16 = 0; c16 < 8; ++c16)
-                st_shared_v4(stg_row + ((c16 ^ (rl & 7)) << 4),
-                             __float_as_uint(__uint_as_float(r[q][4 * c16]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 1]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 2]) * a.scale),
-                             __float_as_uint(__uint_as_float(r[q][4 * c16 + 3]) * a.scale));
+              for (int c4 = 0; c4 < 4; ++c4)
+                st_shared_v4(buf + rl * 64 + ((c4 ^ ((rl >> 1) & 3)) << 4),
+                             __float_as_uint(__uint_as_float(v[4 * c4]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 3]) * a.scale));
               fence_proxy_async_smem();
               named_bar_sync(1, 128);
               if (rl == 0) {
-                tma_reduce_add_5d(&tm_dq, sStage, q * 32, h, t * 128, c, b);
+                tma_reduce_add_5d(&tm_dq, buf, q * 16, h, t * 128, c, b);
                 bulk_commit();
               }
             }

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_before();
           mbar_arrive(bar(B_PFULL + s));
           if (r == 0) BD_TRACE_EVENT(60 + s, int(tcount));  // softmax: P stored
-          if (lane == 0) BD_TRACE_EVENT(40 + 8 + 4 * s + quarter, int(tcount));  // per warp: P stored
+          if (lane == 0) BD_TRACE_EVENT(4 * s + quarter, int(tcount));  // per warp: P stored
         }
         if (!ok) break;
         if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;

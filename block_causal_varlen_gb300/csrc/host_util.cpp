@@ -45,7 +45,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
-                         const char* name, int esize, CUtensorMapDataType dtype, cuuint32_t box0) {
+                         const char* name, int esize, CUtensorMapDataType dtype, cuuint32_t box0,
+                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return fail(BD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
   auto fix = [esize](int64_t stride_elems, int64_t ext, int64_t fallback) {
@@ -59,15 +60,15 @@ static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_
   cuuint64_t strides[4] = {cuuint64_t(sh), cuuint64_t(sr), cuuint64_t(sc), cuuint64_t(sb)};
   cuuint32_t box[5] = {box0, 1, 128, 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(map, dtype, 5, t->ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dtype, 5, t->ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(BD_ERR_ALIGN, "%s: cuTensorMapEncodeTiled failed (%d)", name, int(r));
   return BD_OK;
 }
 
 int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
                              const char* name) {
-  return make_tmap(map, t, B, C, heads, d, name, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32);
+  return make_tmap(map, t, B, C, heads, d, name, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 16, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,

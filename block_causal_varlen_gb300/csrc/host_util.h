@@ -21,7 +21,7 @@ int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t 
                        int64_t d, const char* name);
 
 // Encodes a 5-D tiled TMA map over fp32 [B, C, rows, heads, d] with a box of
-// 128 rows x 32 columns of one head, 128-byte swizzle (for reduce-adds).
+// 128 rows x 16 columns of one head, 64-byte swizzle (for reduce-adds).
 int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
                              const char* name);
 
