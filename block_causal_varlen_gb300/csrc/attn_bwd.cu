@@ -12,7 +12,8 @@
 // shared (all-gathered) K/V buffer, over every chunk of the sequence: that sum
 // is the reduce-scatter SUM done in place.
 //
-// Design (one persistent CTA per SM, 16 warps). A work unit is one 128-row
+// Design (one persistent CTA per SM, 16 warps, each claiming its next work unit
+// from a per-launch counter when it is ready for it). A work unit is one 128-row
 // K/V tile of one K/V head; K and V stay in shared memory while the CTA walks
 // every (query tile, query head of the group) step that attends to the tile.
 //   warp 0       TMA producer: K/V once per unit; per step a Q tile (2-stage
@@ -79,8 +80,12 @@ struct BwdCfg {
 
 enum : int {
   C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_DOFULL, C_DOEMPTY, C_SFULL, C_DPFULL,
-  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_ACCEMPTY, C_DRAIN, C_COUNT
+  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_ACCEMPTY, C_DRAIN, C_UFULL,
+  C_UEMPTY = C_UFULL + kUnitSlots, C_COUNT = C_UEMPTY + kUnitSlots
 };
+// warps that read each claimed unit from the ring: MMA thread, 8 P/dS warps, 4 dQ warps
+constexpr uint32_t kUnitConsumers = 1 + 8 + 4;
+static_assert(8 * C_COUNT + 16 + 4 * kUnitSlots <= 256, "barriers, TMEM slot, abort flag and unit ring overflow their region");
 
 // Iterates the (item, query tile, head) steps of a backward work unit in the
 // same order for every role.
@@ -113,6 +118,8 @@ __global__ void __launch_bounds__(512, 1)
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * C_COUNT + 8);
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT + 16);
+  int* claim = const_cast<int32_t*>(a.plan) + H_BWD_CLAIM;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -122,7 +129,10 @@ __global__ void __launch_bounds__(512, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C_COUNT; ++i) {
-      const uint32_t n = (i == C_PREADY || i == C_DSREADY) ? 256u : (i == C_DQEMPTY || i == C_ACCEMPTY) ? 128u : 1u;
+      const uint32_t n = (i == C_PREADY || i == C_DSREADY)       ? 256u
+                         : (i == C_DQEMPTY || i == C_ACCEMPTY)     ? 128u
+                         : (i >= C_UEMPTY && i < C_UEMPTY + kUnitSlots) ? kUnitConsumers
+                                                                       : 1u;
       mbar_init(bar(i), n);
     }
     *abort_flag = 0;
@@ -149,7 +159,10 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tm_do);
       uint32_t u = 0, sc = 0, q_iss = 0, do_iss = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      for (uint32_t uk = 0; ok; ++uk) {
+        const int w = unit_publish(bar(C_UFULL), bar(C_UEMPTY), unit_ring, claim, a.n_work, uk, abort_flag);
+        if (w == -2) ok = false;
+        if (w < 0) break;
         const int32_t* W = work + w * kBwdWords;
         if (W[W_NQ] == 0) continue;
         const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
@@ -227,7 +240,10 @@ __global__ void __launch_bounds__(512, 1)
       auto mnstep = [](int kk) { return uint32_t((kk * 2048) >> 4); };
       uint32_t u = 0, sc = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      for (uint32_t uk = 0; ok; ++uk) {
+        const int w = unit_take(bar(C_UFULL), bar(C_UEMPTY), unit_ring, uk, abort_flag, true);
+        if (w == -2) ok = false;
+        if (w < 0) break;
         const int32_t* W = work + w * kBwdWords;
         const int nsteps = W[W_NQ];
         if (nsteps == 0) continue;
@@ -308,7 +324,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     uint32_t sc = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+    for (uint32_t uk = 0; ok; ++uk) {
+      const int w = unit_take(bar(C_UFULL), bar(C_UEMPTY), unit_ring, uk, abort_flag, false);
+      if (w == -2) ok = false;
+      if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
       if (W[W_NQ] == 0) continue;
       const int32_t* I0 = items + W[W_ITEM_LO] * kItemWords;
@@ -416,7 +435,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     uint32_t u = 0, sc = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+    for (uint32_t uk = 0; ok; ++uk) {
+      const int w = unit_take(bar(C_UFULL), bar(C_UEMPTY), unit_ring, uk, abort_flag, false);
+      if (w == -2) ok = false;
+      if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
       const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
       const int brow = W[W_KTILE] * 128 + rl;  // buffer row of this lane's key
@@ -532,9 +554,12 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag) {
-    atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
-    atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 2);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) {
+      atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
+      atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 2);
+    }
+    unit_counters_release(claim, const_cast<int32_t*>(plan) + H_BWD_DONE);
   }
 }
 

@@ -6,7 +6,9 @@
 // i's own document with j <= i, plus LSE_i (natural log, fp32). Rows past the
 // valid length give O = 0 and LSE = -inf.
 //
-// Design (one persistent CTA per SM, 12 warps):
+// Design (one persistent CTA per SM, 12 warps; each CTA claims its next work
+// unit from a per-launch counter when it is ready for it, so the units, listed
+// longest first, spread evenly however long each one is):
 //   warp 0      TMA producer: Q tiles of the two query heads, then a ring of
 //               K/V tiles (128 keys x d) for the work unit's key-tile range
 //               [kt_lo, kt_lo + nt); fully masked tiles are never loaded.
@@ -69,8 +71,10 @@ struct FwdCfg {
 // barrier indices (8 bytes each)
 enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14, B_SFULL = 18,
-  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_COUNT = 27
+  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_UFULL = 27, B_UEMPTY = 27 + kUnitSlots,
+  B_COUNT = 27 + 2 * kUnitSlots
 };
+static_assert(8 * B_COUNT + 16 + 4 * kUnitSlots <= 512, "barriers, TMEM slot, abort flag and unit ring overflow their region");
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -86,6 +90,8 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * B_COUNT + 8);
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT + 16);
+  int* claim = const_cast<int32_t*>(a.plan) + H_FWD_CLAIM;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -113,6 +119,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(B_OEMPTY + s), 128);
     }
     mbar_init(bar(B_DRAIN), 1);
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar(B_UFULL + s), 1);
+      mbar_init(bar(B_UEMPTY + s), 1 + 4 * slots);  // the MMA thread and each active softmax warp
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -136,7 +146,10 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_v);
       uint32_t k_it = 0, v_it = 0, qi = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      for (uint32_t uk = 0; ok; ++uk) {
+        const int w = unit_publish(bar(B_UFULL), bar(B_UEMPTY), unit_ring, claim, a.n_work, uk, abort_flag);
+        if (w == -2) ok = false;
+        if (w < 0) break;
         const int32_t* W = work + w * kFwdWords;
         const int nt = W[F_NT];
         if (nt == 0) continue;
@@ -208,7 +221,10 @@ __global__ void __launch_bounds__(384, 1)
       };
       uint32_t kv_it = 0, qi = 0, tcount = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      for (uint32_t uk = 0; ok; ++uk) {
+        const int w = unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, uk, abort_flag, true);
+        if (w == -2) ok = false;
+        if (w < 0) break;
         const int nt = work[w * kFwdWords + F_NT];
         if (nt == 0) continue;
         if (!(ok = mbar_wait(bar(B_QFULL), qi & 1, abort_flag))) break;
@@ -274,7 +290,10 @@ __global__ void __launch_bounds__(384, 1)
     if (s < slots) {
       uint32_t tcount = 0, qi = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < a.n_work && ok; w += gridDim.x) {
+      for (uint32_t uk = 0; ok; ++uk) {
+        const int w = unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, uk, abort_flag, false);
+        if (w == -2) ok = false;
+        if (w < 0) break;
         const int32_t* W = work + w * kFwdWords;
         const int nt = W[F_NT];
         const int32_t* I = items + W[F_ITEM] * kItemWords;
@@ -415,9 +434,12 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag) {
-    atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
-    atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 1);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) {
+      atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
+      atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 1);
+    }
+    unit_counters_release(claim, const_cast<int32_t*>(plan) + H_FWD_DONE);
   }
 }
 

@@ -330,13 +330,14 @@ int32_t build(const bd_plan_desc* d, Built* out) {
       }
     }
   }
-  // Units of one (K/V head, K/V buffer) read the same Q / dO tiles and add into the
-  // same dQ tiles: keep them together so that the CTAs running at the same time
-  // share those tiles in L2; longest first within a group.
+  // CTAs claim units in list order as they finish the previous one, so the list
+  // runs longest first (longest-processing-time order: the last units to start
+  // are the short ones); ties stay grouped by (K/V head, buffer), whose units
+  // read the same Q / dO tiles.
   std::stable_sort(bw.begin(), bw.end(), [](const BW& x, const BW& y) {
+    if (x.w[W_NQ] != y.w[W_NQ]) return x.w[W_NQ] > y.w[W_NQ];
     if (x.w[W_G] != y.w[W_G]) return x.w[W_G] < y.w[W_G];
-    if (x.w[W_BUF] != y.w[W_BUF]) return x.w[W_BUF] < y.w[W_BUF];
-    return x.w[W_NQ] > y.w[W_NQ];
+    return x.w[W_BUF] < y.w[W_BUF];
   });
   for (const BW& w : bw) P.bwd.insert(P.bwd.end(), w.w, w.w + kBwdWords);
   return BD_OK;

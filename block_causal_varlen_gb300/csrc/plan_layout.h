@@ -20,6 +20,10 @@ enum : int {
                         // document, kRowInvalid for padding rows
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
   H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
+  H_FWD_CLAIM = 58,     // forward work-unit claim counter (0 between launches)
+  H_FWD_DONE = 59,      // forward CTAs finished in the current launch
+  H_BWD_CLAIM = 60,     // the same two counters for the backward main kernel
+  H_BWD_DONE = 61,
   kHdrWords = 64
 };
 

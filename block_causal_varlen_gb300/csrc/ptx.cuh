@@ -89,6 +89,45 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// ---- dynamic work distribution of the persistent kernels
+// Work units are claimed one at a time from a per-launch counter in the plan by
+// the producer thread and handed, in claim order, to every other role through a
+// ring of kUnitSlots entries in shared memory (a full and an empty barrier per
+// entry; the empty barrier counts one arrival per consuming warp or thread).
+// -1 marks the end of the work; -2 is returned after a wait timed out.
+constexpr int kUnitSlots = 4;
+__device__ __forceinline__ int unit_publish(uint32_t full0, uint32_t empty0, volatile int32_t* ring, int* claim,
+                                            int n_work, uint32_t k, volatile int* abort) {
+  const int s = int(k % kUnitSlots);
+  if (!mbar_wait(empty0 + 8u * s, ((k / kUnitSlots) & 1) ^ 1, abort)) return -2;
+  int w = atomicAdd(claim, 1);
+  if (w >= n_work) w = -1;
+  ring[s] = w;
+  mbar_arrive(full0 + 8u * s);
+  return w;
+}
+// Every lane of a warp (or a lone thread with one_thread set) reads entry k;
+// one arrival per warp releases it.
+__device__ __forceinline__ int unit_take(uint32_t full0, uint32_t empty0, const volatile int32_t* ring, uint32_t k,
+                                         volatile int* abort, bool one_thread) {
+  const int s = int(k % kUnitSlots);
+  const bool ok = mbar_wait(full0 + 8u * s, (k / kUnitSlots) & 1, abort);
+  const int w = ok ? ring[s] : -2;
+  if (!one_thread) __syncwarp();
+  if (ok && (one_thread || (threadIdx.x & 31) == 0)) mbar_arrive(empty0 + 8u * s);
+  return w;
+}
+// Called by one thread per CTA after the CTA's last use of the counters: the last
+// CTA of the launch resets them for the next launch on the stream.
+__device__ __forceinline__ void unit_counters_release(int* claim, int* done) {
+  __threadfence();
+  if (atomicAdd(done, 1) == int(gridDim.x) - 1) {
+    atomicExch(claim, 0);
+    atomicExch(done, 0);
+  }
+}
+
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -167,8 +167,12 @@ BD_API int32_t bd_plan_bytes(const bd_plan_desc* desc, size_t* bytes);
 /* Build the plan blob into caller-owned host memory `blob` (16-byte aligned,
  * blob_bytes >= bd_plan_bytes). The caller copies the same bytes once per step
  * to device memory (16-byte aligned, writable: kernels record a failure
- * status in it) and passes both copies to the attention calls, which size
- * their launches from the host copy and read the device copy. */
+ * status in it, and the forward and backward-main kernels keep their work-unit
+ * claim counters in it, which the last CTA of each launch returns to zero) and
+ * passes both copies to the attention calls, which size their launches from
+ * the host copy and read the device copy. Launches of the same kernel that
+ * share one device copy must therefore be ordered (one stream, or events):
+ * two of them running at once would take units from each other. */
 BD_API int32_t bd_plan_build(const bd_plan_desc* desc, void* blob, size_t blob_bytes);
 
 /* Read back the header of chunk item `item` (item = b*nchunks + c) and its
