@@ -196,3 +196,34 @@ def test_bwd_dkv_deterministic():
     b = run_bwd(wl, q, k, v, do, 0)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert gu.max_rel(a[0], b[0]) <= 1e-5   # dQ sums in arrival order
+
+
+def test_claim_counters_reset_between_launches():
+    """The forward and backward-main kernels take work units from claim counters
+    in the device plan; the last CTA of each launch returns them to zero, so the
+    same uploaded plan serves launch after launch with identical results."""
+    wl = workloads.config(2)
+    q, k, v, do = workloads.tensors(wl)
+    mode = bd.BD_KV_WINDOW
+    plan, out1, lse1, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, mode)
+    ctr = slice(58, 62)  # forward claim/done, backward claim/done
+    assert torch.count_nonzero(plan.dev[ctr]).item() == 0
+    out2 = torch.empty_like(out1)
+    lse2 = torch.empty_like(lse1)
+    bd.bd_attn_fwd(plan, qd, kd, vd, out2, lse2)
+    dod = gu.as_chunks(do.cuda(), wl.cp)
+    ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
+    grads = []
+    for _ in range(2):
+        dq = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+        dk = torch.zeros(kd.shape, dtype=torch.float32, device="cuda")  # window rows past kv_end stay unwritten
+        dv = torch.zeros_like(dk)
+        bd.bd_attn_bwd(plan, qd, kd, vd, out1, dod, lse1, dq, dk, dv, ws)
+        grads.append((dq, dk, dv))
+    torch.cuda.synchronize()
+    bd.bd_check_status(plan)
+    assert torch.count_nonzero(plan.dev[ctr]).item() == 0
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    (dq1, dk1, dv1), (dq2, dk2, dv2) = grads
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # dK/dV accumulate in TMEM: deterministic
+    assert gu.max_rel(dq2, dq1) < 1e-5                        # dQ adds in arrival order
