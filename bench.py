@@ -119,22 +119,33 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
-KERNEL_SOURCES = {"bd_fwd_kernel": "attn_fwd.cu", "bd_bwd_kernel": "attn_bwd.cu"}
+# the sources each timed kernel is compiled from (its own file and the headers it includes)
+KERNEL_SOURCES = {
+    "bd_fwd_kernel": ("attn_fwd.cu", "ptx.cuh", "plan_layout.h", "host_util.h", "common.h"),
+    "bd_bwd_kernel": ("attn_bwd.cu", "ptx.cuh", "plan_layout.h", "host_util.h", "common.h", "bwd_aux.h"),
+}
+
+
+def kernel_source_digest(kernel):
+    """sha256 over the kernel's source files, in the listed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_causal_varlen_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def kernel_traffic(kernel, workload):
     """DRAM bytes per launch (read + write) of `kernel` on `workload` from the ncu
     capture recorded in profiles/traffic.json, or None when there is none or the
-    kernel's source changed since the counters were taken."""
-    import hashlib
+    kernel's sources changed since the counters were taken."""
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(prof) or kernel not in KERNEL_SOURCES:
         return None
     try:
         rec = json.load(open(prof)).get(f"{kernel}:{workload}")
-        src = os.path.join(ROOT, "block_causal_varlen_gb300", "csrc", KERNEL_SOURCES[kernel])
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec and rec.get("source_sha256") == digest:
+        if rec and rec.get("source_sha256") == kernel_source_digest(kernel):
             return rec.get("bytes")
     except Exception:
         pass
