@@ -80,7 +80,7 @@ struct BwdCfg {
 
 enum : int {
   C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_DOFULL, C_DOEMPTY, C_SFULL, C_DPFULL,
-  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_ACCEMPTY, C_DRAIN, C_UFULL,
+  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_DVFREE, C_DKFREE, C_DRAIN, C_UFULL,
   C_UEMPTY = C_UFULL + kUnitSlots, C_COUNT = C_UEMPTY + kUnitSlots
 };
 // warps that read each claimed unit from the ring: MMA thread, 8 P/dS warps, 4 dQ warps
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C_COUNT; ++i) {
       const uint32_t n = (i == C_PREADY || i == C_DSREADY)       ? 256u
-                         : (i == C_DQEMPTY || i == C_ACCEMPTY)     ? 128u
+                         : (i == C_DQEMPTY || i == C_DVFREE || i == C_DKFREE) ? 128u
                          : (i >= C_UEMPTY && i < C_UEMPTY + kUnitSlots) ? kUnitConsumers
                                                                        : 1u;
       mbar_init(bar(i), n);
@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(512, 1)
           tc_commit(bar(C_DPFULL));
           BD_TRACE_EVENT(3, int(sc));  // MMA: waits P
           if (!(ok = mbar_wait(bar(C_PREADY), sc & 1, abort_flag))) break;
-          if (s == 0 && !(ok = mbar_wait(bar(C_ACCEMPTY), (u & 1) ^ 1, abort_flag))) break;
+          // a unit's first dV / dK overwrite the accumulators the previous unit's
+          // epilogue reads out of TMEM
+          if (s == 0 && !(ok = mbar_wait(bar(C_DVFREE), (u & 1) ^ 1, abort_flag))) break;
           BD_TRACE_EVENT(4, int(sc));  // MMA: dV issue
           tc_fence_after();
 #pragma unroll
@@ -281,9 +283,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_commit(bar(C_DOEMPTY));
           // the next step's scores go ahead of this step's dK / dQ so that the
           // P^T warps can start on them while the tensor core finishes this step
-          // (P^T of this step, in the same TMEM columns, was read by dV above);
-          // if its Q tile has not landed yet they go after dQ, else after dK, so
-          // that a late Q never holds up this step's own MMAs
+          // (P^T of this step, in the same TMEM columns, was read by dV above)
           if (s + 1 < nsteps) {
             if (!(ok = mbar_wait(bar(C_QFULL0 + ((sc + 1) & 1)), ((sc + 1) >> 1) & 1, abort_flag))) break;
             tc_fence_after();
@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(512, 1)
           BD_TRACE_EVENT(5, int(sc));  // MMA: waits dS
           if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
           BD_TRACE_EVENT(6, int(sc));  // MMA: dQ/dK issue
+          if (s == 0 && !(ok = mbar_wait(bar(C_DKFREE), (u & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
           // dQ first: its drain gates the next step's dP^T (same TMEM columns)
 #pragma unroll
@@ -513,36 +514,36 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) break;
       if (!(ok = mbar_wait(bar(C_ACCDONE), u & 1, abort_flag))) break;
       tc_fence_after();
+      // dV, then dK (x scale): each block leaves TMEM whole before it is stored, so
+      // that the next unit's first dV / dK MMA can start while the rows go out
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t rv[32], rk[32];
-        tmem_ld32(tmem + lane_base + Cfg::kColDV + q * 32, rv);
-        tmem_ld32(tmem + lane_base + Cfg::kColDK + q * 32, rk);
-        tmem_ld_wait();
-        reg_fence(rv);
-        reg_fence(rk);
-        if (krow_ok) {
+      for (int x = 0; x < 2; ++x) {
+        uint32_t v[D / 32][32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 vv = make_float4(__uint_as_float(rv[4 * e]), __uint_as_float(rv[4 * e + 1]),
-                                    __uint_as_float(rv[4 * e + 2]), __uint_as_float(rv[4 * e + 3]));
-            float4 kv = make_float4(__uint_as_float(rk[4 * e]) * a.scale, __uint_as_float(rk[4 * e + 1]) * a.scale,
-                                    __uint_as_float(rk[4 * e + 2]) * a.scale,
-                                    __uint_as_float(rk[4 * e + 3]) * a.scale);
-            float4* pv = reinterpret_cast<float4*>(dvrow + q * 32) + e;
-            float4* pk = reinterpret_cast<float4*>(dkrow + q * 32) + e;
-            if (a.accumulate) {
-              const float4 ov = *pv, ok4 = *pk;
-              vv.x += ov.x; vv.y += ov.y; vv.z += ov.z; vv.w += ov.w;
-              kv.x += ok4.x; kv.y += ok4.y; kv.z += ok4.z; kv.w += ok4.w;
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + (x ? Cfg::kColDK : Cfg::kColDV) + q * 32, v[q]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) reg_fence(v[q]);
+        tc_fence_before();
+        mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
+        if (krow_ok) {
+          float* row = x ? dkrow : dvrow;
+          const float mul = x ? a.scale : 1.f;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
+                                     __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
+              float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
+              if (a.accumulate) {
+                const float4 old = *p;
+                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              }
+              *p = o;
             }
-            *pv = vv;
-            *pk = kv;
-          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C_ACCEMPTY));
       ++u;
     }
     if (rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed

@@ -51,7 +51,7 @@ struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16
   // K and V have rings of their own: a K tile is released as soon as both
   // slots' S MMAs have read it, so it can be refilled well ahead of its use.
-  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
@@ -167,13 +167,17 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < nt; ++j) {
           const int row = (W[F_KTLO] + j) * 128 - kvbase;
           const int sk = k_it % NK, sv = v_it % NV;
+          BD_TRACE_EVENT(24, int(k_it));  // producer: waits for a K stage
           if (!(ok = mbar_wait(bar(B_KEMPTY + sk), ((k_it / NK) & 1) ^ 1, abort_flag))) break;
+          BD_TRACE_EVENT(23, int(k_it));  // producer: K load issued
           mbar_expect_tx(bar(B_KFULL + sk), Cfg::kTileBytes);
           for (int hf = 0; hf < D / 64; ++hf)
             tma_load_5d(sK + sk * Cfg::kTileBytes + hf * 16384, &tm_k, bar(B_KFULL + sk), hf * 64, g, row, kc,
                         kb);
           ++k_it;
+          BD_TRACE_EVENT(25, int(v_it));  // producer: waits for a V stage
           if (!(ok = mbar_wait(bar(B_VEMPTY + sv), ((v_it / NV) & 1) ^ 1, abort_flag))) break;
+          BD_TRACE_EVENT(22, int(v_it));  // producer: V load issued
           mbar_expect_tx(bar(B_VFULL + sv), Cfg::kTileBytes);
           for (int hf = 0; hf < D / 64; ++hf)
             tma_load_5d(sV + sv * Cfg::kTileBytes + hf * 16384, &tm_v, bar(B_VFULL + sv), hf * 64, g, row, kc,
@@ -246,7 +250,9 @@ __global__ void __launch_bounds__(384, 1)
           const int svp = itp % NV, skn = itn % NK;
           const uint32_t tp = tcount + j - 1;
           if (j < nt && !(ok = mbar_wait(bar(B_KFULL + skn), (itn / NK) & 1, abort_flag))) break;
+          BD_TRACE_EVENT(18, int(tp));  // MMA: next K tile present
           if (!(ok = mbar_wait(bar(B_VFULL + svp), (itp / NV) & 1, abort_flag))) break;
+          BD_TRACE_EVENT(19, int(tp));  // MMA: V tile present
           for (int s = 0; s < slots; ++s) {
             BD_TRACE_EVENT(14 + s, int(tp));  // MMA: starts waiting for P
             if (!(ok = mbar_wait(bar(B_PFULL + s), tp & 1, abort_flag))) break;
@@ -278,6 +284,22 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
    }
+#ifdef BD_TRACE
+   else if ((warp == 2 || warp == 3) && lane == 0 && blockIdx.x == 0) {
+    // tracing build only: stamp the moment each K (warp 2) / V (warp 3) tile lands
+    const bool isk = warp == 2;
+    const int n = isk ? NK : NV;
+    for (uint32_t it = 0; it < uint32_t(kTraceTiles); ++it) {
+      const uint32_t fb = bar((isk ? B_KFULL : B_VFULL) + int(it % n)), par = (it / n) & 1;
+      const uint64_t t0 = globaltimer();
+      bool got = false;
+      while (!(got = mbar_try_wait(fb, par)) && globaltimer() - t0 < 20000000ull) {
+      }
+      if (!got) break;
+      BD_TRACE_EVENT(isk ? 26 : 27, int(it));
+    }
+   }
+#endif
   } else {
     regs_set<Cfg::kRegsSoftmax, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ softmax
