@@ -22,7 +22,10 @@ packed sequences":
   K longer than Q, aligned bottom-right (Key correctness property 2);
 * the backward of the fused K/V all-gather is a reduce-scatter SUM, i.e. the
   per-chunk dK/dV partials add up at their owners (Design overview,
-  exchange.py).
+  exchange.py);
+* attention dropout, which the page forwards to the native kernels (Proof,
+  GPU varlen tests), is standard dropout on the normalised probabilities with a
+  counter-based keep mask (``dropout.py``).
 
 Floating point runs in float64 unless a caller asks for another dtype. The
 pieces are pinned by ``tests/test_oracle.py`` and ``tests/test_segment.py``
@@ -33,4 +36,8 @@ from .exchange import doc_ids_to_cu, exchange_plan  # noqa: F401
 from .attention import (  # noqa: F401
     block_causal_mask, attention_fwd, attention_bwd, chunk_fwd, chunk_bwd,
     attention_bwd_cols, attention_bwd_rows,
+)
+from .dropout import (  # noqa: F401
+    philox4x32_10, keep_threshold, keep_mask, attention_fwd_dropout, attention_bwd_dropout,
+    chunk_fwd_dropout, chunk_bwd_dropout,
 )
