@@ -17,9 +17,12 @@ the mask the forward used:
 
 (D_i = sum_k P'_ik dP_ik = <dO_i, O_i> because O is the dropped output.)
 
-u_ij is word (j mod 4) of Philox4x32-10 at counter (j // 4, i, h, b) under the
-key (seed mod 2**32, seed // 2**32), with i the query row and j the key row of
-sequence b in global (sequence) rows and h the query head. Philox4x32-10 is
+u_ij is word 2 (i mod 2) + (j mod 2) of Philox4x32-10 at counter
+(j // 2, i // 2, h, b) under the key (seed mod 2**32, seed // 2**32), with i the
+query row and j the key row of sequence b in global (sequence) rows and h the
+query head: one call covers a 2 x 2 block of (query, key) pairs, so a thread
+that walks keys of one row and a thread that walks queries of one key both use
+two of each call's four words. Philox4x32-10 is
 written from its published definition (Salmon, Moraes, Dror and Shaw,
 "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011): ten rounds of
 
@@ -73,16 +76,17 @@ def keep_mask(b: int, h: int, rows, cols, seed: int, p: float) -> torch.Tensor:
     t = keep_threshold(p)
     if t == 0:
         return torch.ones(len(rows), len(cols), dtype=torch.bool)
-    blocks = np.unique(cols // 4)
-    cnt = np.zeros((len(rows), len(blocks), 4), dtype=np.uint64)
-    cnt[:, :, 0] = blocks[None, :]
-    cnt[:, :, 1] = rows[:, None]
+    rb, cb = np.unique(rows // 2), np.unique(cols // 2)
+    cnt = np.zeros((len(rb), len(cb), 4), dtype=np.uint64)
+    cnt[:, :, 0] = cb[None, :]
+    cnt[:, :, 1] = rb[:, None]
     cnt[:, :, 2] = h
     cnt[:, :, 3] = b
     words = philox4x32_10(cnt.reshape(-1, 4), (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
-    words = words.reshape(len(rows), len(blocks), 4)
-    bi = np.searchsorted(blocks, cols // 4)
-    u = words[:, bi, cols % 4]                                   # [R, C]
+    words = words.reshape(len(rb), len(cb), 4)
+    ri = np.searchsorted(rb, rows // 2)[:, None]
+    ci = np.searchsorted(cb, cols // 2)[None, :]
+    u = words[ri, ci, 2 * (rows % 2)[:, None] + (cols % 2)[None, :]]      # [R, C]
     return torch.from_numpy(u >= np.uint32(t))
 
 

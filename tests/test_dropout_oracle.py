@@ -80,9 +80,22 @@ def test_mask_depends_on_every_counter_and_key_word():
         args.update(kw)
         other = oracle.keep_mask(args["b"], args["h"], np.arange(64), np.arange(64), args["seed"], 0.5)
         assert not torch.equal(base, other), kw
-    # rows and the 4-key blocks are separate counter words
-    assert not torch.equal(base[0], base[1])
-    assert not torch.equal(base[:, :4], base[:, 4:8])
+    # neighbouring rows and key blocks draw different words
+    assert not torch.equal(base[0], base[1]) and not torch.equal(base[0], base[2])
+    assert not torch.equal(base[:, :2], base[:, 2:4])
+
+
+def test_mask_layout_is_the_documented_counter_and_word():
+    """keep[i, j] uses word 2 (i mod 2) + (j mod 2) of the call at counter (j // 2, i // 2, h, b)."""
+    seed, p, b, h = 0xABCDEF0123, 0.5, 3, 7
+    rows, cols = np.array([0, 1, 5, 6, 1000]), np.array([0, 1, 2, 9, 4097])
+    m = oracle.keep_mask(b, h, rows, cols, seed, p)
+    t = oracle.keep_threshold(p)
+    for a, i in enumerate(rows):
+        for c, j in enumerate(cols):
+            w = oracle.philox4x32_10(np.array([[j // 2, i // 2, h, b]], dtype=np.uint64),
+                                     (seed & 0xFFFFFFFF, seed >> 32))[0]
+            assert bool(m[a, c]) == (int(w[2 * (i % 2) + j % 2]) >= t)
 
 
 def _autograd_reference(cu, S, H, Hkv, p, seed, b, d=8):
