@@ -122,6 +122,12 @@ class Plan:
         self.dev.copy_(src, non_blocking=non_blocking)
         return self
 
+    def set_dropout(self, p: float, seed: int):
+        """Attention dropout with probability p (0 turns it off) and a 64-bit seed,
+        written into the host blob: upload the plan again before the next launch."""
+        check(load().bd_plan_set_dropout(self.host_ptr, float(p), int(seed) & (2 ** 64 - 1)))
+        return self
+
     def useful_pairs(self) -> int:
         """Unmasked (query, key) pairs per head over the whole plan."""
         return int(load().bd_plan_useful_pairs(self.host_ptr))

@@ -76,6 +76,7 @@ EXPORTS = {
     "bd_plan_chunk": (C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(bd_chunk_hdr), C.POINTER(bd_segment_t),
                                   C.c_int32]),
     "bd_plan_useful_pairs": (C.c_int64, [C.c_void_p]),
+    "bd_plan_set_dropout": (C.c_int32, [C.c_void_p, C.c_double, C.c_uint64]),
     "bd_attn_fwd": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                 C.POINTER(bd_tensor), C.c_int32, C.POINTER(bd_tensor), C.POINTER(bd_rowstat),
                                 C.c_void_p]),

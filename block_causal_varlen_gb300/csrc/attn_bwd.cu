@@ -54,6 +54,9 @@ struct BwdArgs {
   int64_t v_sb, v_sc, v_sr, v_sh;
   int32_t L, Lpad, H, G, Ck, n_work, accumulate, dk_rows;
   float scale, scale_log2;
+  // attention dropout (used by the DROP instantiation): keep iff Philox word >= thresh
+  uint32_t drop_thresh, drop_k0, drop_k1;
+  float drop_scale;
 };
 
 template <int D>
@@ -103,7 +106,7 @@ struct StepRange {
   }
 };
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(512, 1)
     bd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -337,9 +340,11 @@ __global__ void __launch_bounds__(512, 1)
       for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
         int t0, t1, r0;
         if (!R.tiles(it, t0, t1, r0)) continue;
+        const uint32_t bseq = uint32_t(items[it * kItemWords + I_B]);
         for (int t = t0; t <= t1 && ok; ++t)
           for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
             const int qs = sc & 1;
+            const uint32_t hq = uint32_t(W[W_G] * a.G + hh);  // query head
             const int i0 = r0 + t * 128;  // global row of query column 0
             const float* st_lse = reinterpret_cast<const float*>(smem + Cfg::kOffStat + qs * Cfg::kStatBytes);
             const float* st_d = st_lse + 128;
@@ -356,6 +361,7 @@ __global__ void __launch_bounds__(512, 1)
             // P^T is kept as the bf16 pairs written to TMEM (the dV MMA reads the same
             // rounded values); dS below unpacks them
             uint32_t pk[2][16];
+            uint32_t keep[2] = {0u, 0u};  // dropout: bit e of chunk ch keeps query i0 + ib + e
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
               uint32_t r[32];
@@ -381,7 +387,40 @@ __global__ void __launch_bounds__(512, 1)
               }
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[ch][e] = pack_bf16(p[2 * e], p[2 * e + 1]);
-              tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk[ch]);
+              if constexpr (DROP) {
+                // keep bits of queries ibase .. ibase + 31 for this key: one Philox call
+                // per 2-query block (word 2 (i mod 2) + (j mod 2) of counter (j/2, i/2, h, b))
+                const int ibase = i0 + ib;
+                uint32_t kb = 0;
+                if ((ibase & 1) == 0) {
+#pragma unroll
+                  for (int e2 = 0; e2 < 16; ++e2) {
+                    const uint4 rr = philox4x32_10(
+                        make_uint4(uint32_t(j) >> 1, uint32_t(ibase >> 1) + e2, hq, bseq), a.drop_k0, a.drop_k1);
+                    const uint32_t w0 = (j & 1) ? rr.y : rr.x, w1 = (j & 1) ? rr.w : rr.z;
+                    kb |= (uint32_t(w0 >= a.drop_thresh) << (2 * e2)) | (uint32_t(w1 >= a.drop_thresh) << (2 * e2 + 1));
+                  }
+                } else {
+#pragma unroll 4
+                  for (int e = 0; e < 32; ++e) {
+                    const int i = ibase + e;
+                    const uint4 rr = philox4x32_10(make_uint4(uint32_t(j) >> 1, uint32_t(i) >> 1, hq, bseq),
+                                                   a.drop_k0, a.drop_k1);
+                    const uint32_t w = (i & 1) ? ((j & 1) ? rr.w : rr.z) : ((j & 1) ? rr.y : rr.x);
+                    kb |= uint32_t(w >= a.drop_thresh) << e;
+                  }
+                }
+                keep[ch] = kb;
+                // the dV product reads the dropped, rescaled probabilities
+                uint32_t pd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pd[e] = pack_bf16(((kb >> (2 * e)) & 1) ? p[2 * e] * a.drop_scale : 0.f,
+                                    ((kb >> (2 * e + 1)) & 1) ? p[2 * e + 1] * a.drop_scale : 0.f);
+                tmem_st16(tmem + lane_base + half * 64 + ch * 16, pd);
+              } else {
+                tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk[ch]);
+              }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -408,10 +447,17 @@ __global__ void __launch_bounds__(512, 1)
                 const float4 d4 = ld_shared_f4(st_d + ib + 4 * e4);
                 const int e = 4 * e4;
                 const uint32_t p01 = pk[ch][2 * e4], p23 = pk[ch][2 * e4 + 1];
-                const float s0 = __uint_as_float(p01 << 16) * (__uint_as_float(r[e]) - d4.x);
-                const float s1 = __uint_as_float(p01 & 0xffff0000u) * (__uint_as_float(r[e + 1]) - d4.y);
-                const float s2 = __uint_as_float(p23 << 16) * (__uint_as_float(r[e + 2]) - d4.z);
-                const float s3 = __uint_as_float(p23 & 0xffff0000u) * (__uint_as_float(r[e + 3]) - d4.w);
+                float dp[4] = {__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                               __uint_as_float(r[e + 3])};
+                if constexpr (DROP) {
+                  // dS = P (keep dP / (1 - p) - D) with the undropped P
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) dp[k] = ((keep[ch] >> (e + k)) & 1) ? dp[k] * a.drop_scale : 0.f;
+                }
+                const float s0 = __uint_as_float(p01 << 16) * (dp[0] - d4.x);
+                const float s1 = __uint_as_float(p01 & 0xffff0000u) * (dp[1] - d4.y);
+                const float s2 = __uint_as_float(p23 << 16) * (dp[2] - d4.z);
+                const float s3 = __uint_as_float(p23 & 0xffff0000u) * (dp[3] - d4.w);
                 dsk[2 * e4] = pack_bf16(s0, s1);
                 dsk[2 * e4 + 1] = pack_bf16(s2, s3);
               }
@@ -564,7 +610,7 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                           const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdArgs& a, int grid,
                           cudaStream_t stream) {
@@ -573,10 +619,10 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bd_bwd_kernel<D>);
+    e = cudaFuncGetAttributes(&fa, bd_bwd_kernel<D, DROP>);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd)");
     // the setmaxnreg directions were chosen for this launch count: refuse any other
     if (fa.numRegs != Cfg::kRegsLaunch)
@@ -584,7 +630,7 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
                   fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
-  bd_bwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, mdq, a);
+  bd_bwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, mdq, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_bwd_kernel launch");
   return BD_OK;
@@ -724,8 +770,17 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   if ((st = sm_count(&nsm))) return st;
   const int grid = a.n_work < nsm ? a.n_work : nsm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = c.D == 128 ? launch_bwd<128>(mq, mk, mv, mdo, mdq, a, grid, s)
-                  : launch_bwd<64>(mq, mk, mv, mdo, mdq, a, grid, s);
+  a.drop_thresh = uint32_t(pv.hdr(H_DROP_THRESH));
+  a.drop_k0 = uint32_t(pv.hdr(H_DROP_SEED_LO));
+  a.drop_k1 = uint32_t(pv.hdr(H_DROP_SEED_HI));
+  const int32_t dbits = pv.hdr(H_DROP_SCALE_BITS);
+  memcpy(&a.drop_scale, &dbits, 4);
+  if (a.drop_thresh != 0)
+    st = c.D == 128 ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, a, grid, s)
+                    : launch_bwd<64, true>(mq, mk, mv, mdo, mdq, a, grid, s);
+  else
+    st = c.D == 128 ? launch_bwd<128, false>(mq, mk, mv, mdo, mdq, a, grid, s)
+                    : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, a, grid, s);
   if (st) return st;
   return ok();
 }

@@ -44,6 +44,9 @@ struct FwdArgs {
   int64_t l_sb, l_sc, l_sh;
   int32_t L, n_work, slots, Ck;
   float scale_log2;
+  // attention dropout (used by the DROP instantiation): keep iff Philox word >= thresh
+  uint32_t drop_thresh, drop_k0, drop_k1;
+  float drop_scale;
 };
 
 template <int D>
@@ -76,7 +79,7 @@ enum : int {
 };
 static_assert(8 * B_COUNT + 16 + 4 * kUnitSlots <= 512, "barriers, TMEM slot, abort flag and unit ring overflow their region");
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(384, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -407,7 +410,17 @@ __global__ void __launch_bounds__(384, 1)
             t.x = ex2(t.x);
             t.y = ex2(t.y);
             s4[e & 3] = fadd2(s4[e & 3], t);
-            pk[e >> 5][e & 31] = pack_bf16(t.x, t.y);
+            if constexpr (DROP) {
+              // keys c0 + 2e, c0 + 2e + 1 form one 2-key block (c0 is a multiple of 128);
+              // the row sum above keeps the undropped values, 1/(1-p) goes in the epilogue
+              const uint4 rr = philox4x32_10(make_uint4(uint32_t(c0 + 2 * e) >> 1, uint32_t(grow) >> 1,
+                                                        uint32_t(h), uint32_t(b)),
+                                             a.drop_k0, a.drop_k1);
+              const uint32_t u0 = (grow & 1) ? rr.z : rr.x, u1 = (grow & 1) ? rr.w : rr.y;
+              pk[e >> 5][e & 31] = pack_bf16(u0 >= a.drop_thresh ? t.x : 0.f, u1 >= a.drop_thresh ? t.y : 0.f);
+            } else {
+              pk[e >> 5][e & 31] = pack_bf16(t.x, t.y);
+            }
           }
           const float2 s01 = fadd2(s4[0], s4[1]), s23 = fadd2(s4[2], s4[3]);
           const float2 st = fadd2(s01, s23);
@@ -425,7 +438,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
         tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * (DROP ? a.drop_scale : 1.f);
 #pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
           uint32_t ov[32];
@@ -465,7 +478,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
                           int grid, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
@@ -473,10 +486,10 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bd_fwd_kernel<D>);
+    e = cudaFuncGetAttributes(&fa, bd_fwd_kernel<D, DROP>);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
     // setmaxnreg.inc waits until registers are free: never launch a split that cannot be met
     if (fa.numRegs != Cfg::kRegsLaunch)
@@ -484,7 +497,7 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
                   fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
-  bd_fwd_kernel<D><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);
+  bd_fwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_fwd_kernel launch");
   return BD_OK;
@@ -554,7 +567,15 @@ extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, cons
   if ((st = sm_count(&nsm))) return st;
   const int grid = a.n_work < nsm ? a.n_work : nsm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = D == 128 ? launch_fwd<128>(mq, mk, mv, a, grid, s) : launch_fwd<64>(mq, mk, mv, a, grid, s);
+  a.drop_thresh = uint32_t(pv.hdr(H_DROP_THRESH));
+  a.drop_k0 = uint32_t(pv.hdr(H_DROP_SEED_LO));
+  a.drop_k1 = uint32_t(pv.hdr(H_DROP_SEED_HI));
+  const int32_t dbits = pv.hdr(H_DROP_SCALE_BITS);
+  memcpy(&a.drop_scale, &dbits, 4);
+  if (a.drop_thresh != 0)
+    st = D == 128 ? launch_fwd<128, true>(mq, mk, mv, a, grid, s) : launch_fwd<64, true>(mq, mk, mv, a, grid, s);
+  else
+    st = D == 128 ? launch_fwd<128, false>(mq, mk, mv, a, grid, s) : launch_fwd<64, false>(mq, mk, mv, a, grid, s);
   if (st) return st;
   return ok();
 }

@@ -420,6 +420,24 @@ extern "C" int32_t bd_plan_chunk(const void* plan_host, int32_t item, bd_chunk_h
   return ok();
 }
 
+extern "C" int32_t bd_plan_set_dropout(void* plan_host, double p, uint64_t seed) {
+  PlanView pv;
+  int32_t st = view_plan(plan_host, &pv);
+  if (st) return st;
+  if (!(p >= 0.0 && p < 1.0)) return fail(BD_ERR_ARG, "dropout probability %g not in [0, 1)", p);
+  const double t = std::floor(p * 4294967296.0 + 0.5);
+  const uint32_t thresh = t >= 4294967295.0 ? 0xFFFFFFFFu : uint32_t(t);
+  const float scale = float(1.0 / (1.0 - p));
+  int32_t* h = static_cast<int32_t*>(plan_host);
+  int32_t sbits;
+  memcpy(&sbits, &scale, 4);
+  h[H_DROP_THRESH] = int32_t(thresh);
+  h[H_DROP_SCALE_BITS] = sbits;
+  h[H_DROP_SEED_LO] = int32_t(uint32_t(seed & 0xFFFFFFFFu));
+  h[H_DROP_SEED_HI] = int32_t(uint32_t(seed >> 32));
+  return ok();
+}
+
 extern "C" int64_t bd_plan_useful_pairs(const void* plan_host) {
   PlanView pv;
   if (view_plan(plan_host, &pv)) return -1;

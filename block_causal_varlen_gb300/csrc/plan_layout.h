@@ -18,6 +18,10 @@ enum : int {
   H_USEFUL_LO, H_USEFUL_HI, H_NBUF, H_FWD_TILES_LO, H_FWD_TILES_HI,
   H_OFF_ROWDS,          // int32 [nitems][L]: global start row of each chunk row's
                         // document, kRowInvalid for padding rows
+  H_DROP_THRESH,        // attention dropout: keep iff Philox word >= this (uint32; 0 = off)
+  H_DROP_SCALE_BITS,    // 1 / (1 - p) as float bits
+  H_DROP_SEED_LO,       // Philox key words
+  H_DROP_SEED_HI,
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
   H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
   H_FWD_CLAIM = 58,     // forward work-unit claim counter (0 between launches)

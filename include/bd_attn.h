@@ -183,6 +183,19 @@ BD_API int32_t bd_plan_chunk(const void* plan_host, int32_t item, bd_chunk_hdr* 
 /* Useful (unmasked) (query, key) pairs per head over all items of a plan. */
 BD_API int64_t bd_plan_useful_pairs(const void* plan_host);
 
+/* bd_plan_set_dropout -- turn attention dropout on (p > 0) or off (p = 0) in a
+ * host plan blob, before it is copied to the device. The native Flash path the
+ * NeMo Automodel page forwards dropout to (Proof, GPU varlen tests) gives no
+ * formulas; the reading implemented: the forward keeps probability P_ij with
+ * keep_ij = (u_ij >= t), t = floor(p * 2^32 + 1/2) capped at 2^32 - 1, and
+ * computes O = sum_j P_ij keep_ij v_j / (1 - p) with the undropped LSE; the
+ * backward regenerates the same mask (dS_ij = P_ij (keep_ij dP_ij / (1 - p) - D_i),
+ * D_i = <dO_i, O_i>). u_ij is word 2 (i mod 2) + (j mod 2) of Philox4x32-10
+ * (Salmon et al., SC 2011) at counter (j / 2, i / 2, h, b) under the key
+ * (seed mod 2^32, seed / 2^32); i, j are global query / key rows of sequence b
+ * and h the query head. Returns BD_ERR_ARG unless 0 <= p < 1. */
+BD_API int32_t bd_plan_set_dropout(void* plan_host, double p, uint64_t seed);
+
 /* A strided device tensor whose last (head) dimension is contiguous.
  * Query-like tensors (q, out, dout, dq) are [B, nchunks, L, H, d]; key-like
  * tensors (k, v, dk, dv) are [B, Ck, rows, Hkv, d] with Ck = 1 for

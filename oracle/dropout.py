@@ -9,7 +9,7 @@ standard attention dropout on the normalised probabilities, with the keep mask
 drawn from a counter-based generator so that the backward regenerates exactly
 the mask the forward used:
 
-    keep_ij = u_ij >= t,          t = round(p * 2**32)  (p in [0, 1))
+    keep_ij = u_ij >= t,          t = floor(p * 2**32 + 1/2), at most 2**32 - 1 (p in [0, 1))
     P'_ij   = P_ij * keep_ij / (1 - p),   O_i = sum_j P'_ij v_j,   LSE unchanged
     D_i     = <dO_i, O_i>,        dP_ij = <dO_i, v_j>
     dS_ij   = P_ij * (keep_ij * dP_ij / (1 - p) - D_i)
@@ -66,7 +66,7 @@ def keep_threshold(p: float) -> int:
     """The 32-bit threshold t of keep = (u >= t) for dropout probability p in [0, 1)."""
     if not 0.0 <= p < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
-    return min(int(round(p * 2.0 ** 32)), 2 ** 32 - 1)
+    return min(int(math.floor(p * 2.0 ** 32 + 0.5)), 2 ** 32 - 1)
 
 
 def keep_mask(b: int, h: int, rows, cols, seed: int, p: float) -> torch.Tensor:
