@@ -159,7 +159,10 @@ def useful_flops(plan, wl):
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None):
+DROPOUT_SEED = 0x5EED0F0D0F0A77E0  # fixed seed of the --dropout runs
+
+
+def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None, dropout=0.0):
     """Time the oracle (fwd + bwd) on the host cores over the given chunks, one
     K/V head's query heads at a time (heads: how many query heads; with budget_s,
     stop once that many seconds have been spent, after at least one group).
@@ -181,8 +184,15 @@ def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None):
         for g in range((nh + G - 1) // G):
             hq = slice(g * G, min(nh, (g + 1) * G))
             kw, vw = k[b, a:e, g:g + 1], v[b, a:e, g:g + 1]
-            oracle.chunk_fwd(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, kv_base=a)
-            oracle.chunk_bwd(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L, kv_base=a)
+            if dropout > 0:
+                # the head index only selects the keep mask; timing is what matters here
+                oracle.chunk_fwd_dropout(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, dropout, DROPOUT_SEED,
+                                         b=b, kv_base=a)
+                oracle.chunk_bwd_dropout(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L,
+                                         dropout, DROPOUT_SEED, b=b, kv_base=a)
+            else:
+                oracle.chunk_fwd(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, kv_base=a)
+                oracle.chunk_bwd(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L, kv_base=a)
             pairs += n_chunk * (hq.stop - hq.start)
             if budget_s is not None and time.perf_counter() - t0 > budget_s:
                 done = True
@@ -256,7 +266,10 @@ def run_ours(args):
     wl = workloads.config(args.workload)
     mode = bd.BD_KV_WINDOW if wl.kv_mode == "window" else bd.BD_KV_GATHER
     q, k, v, do = workloads.tensors(wl)
-    plan = bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode).upload(dev)
+    plan = bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode)
+    if args.dropout > 0:
+        plan.set_dropout(args.dropout, DROPOUT_SEED)
+    plan.upload(dev)
     n_pairs, f_fwd, f_bwd = useful_flops(plan, wl)
     f_step = f_fwd + f_bwd
 
@@ -421,7 +434,8 @@ def run_ours(args):
     dom_ms = t_main if dominant == "bd_bwd_kernel" else t_fwd
     dom_flops = f_bwd if dominant == "bd_bwd_kernel" else f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = kernel_traffic(dominant, wl.name)
+    # the recorded counters are for the dropout-free instantiation
+    traffic = kernel_traffic(dominant, wl.name) if args.dropout == 0 else None
 
     result = None
     if rank == 0:
@@ -433,7 +447,7 @@ def run_ours(args):
             chunks = [(b0, c) for c in range(wl.cp) if wl.cu[b0][-1] > c * wl.L]
             # cheapest chunks first, one K/V head's query heads at a time, until ~12 s of oracle work
             chunks.sort(key=lambda bc: oracle_cost(wl, *bc))
-            secs, pairs = oracle_sample(wl, q, k, v, do, chunks, budget_s=12.0)
+            secs, pairs = oracle_sample(wl, q, k, v, do, chunks, budget_s=12.0, dropout=args.dropout)
             cpu = {"value": 14.0 * wl.d * pairs / secs / 1e12, "unit": "TFLOP/s", "cores": _t.get_num_threads(),
                    "kind": "oracle", "seconds": secs,
                    "sample": f"oracle fwd+bwd (fp64) on chunks of sequence 0, cheapest first, one K/V head's "
@@ -446,6 +460,7 @@ def run_ours(args):
             "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "L": wl.L, "H": wl.H,
                        "Hkv": wl.Hkv, "d": wl.d, "kv_mode": wl.kv_mode, "layout_seed": wl.seed,
                        "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
+                       "dropout": args.dropout,
                        "l2": "flushed between steps by a 256 MiB write outside the step events"},
             "fwd_tflops": f_fwd / (t_fwd * 1e-3) / 1e12,
             "bwd_tflops": f_bwd / ((t_pre + t_main + t_own) * 1e-3) / 1e12,
@@ -478,6 +493,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="attention dropout probability (default 0, as in every benchmarked configuration)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
