@@ -392,7 +392,22 @@ __global__ void __launch_bounds__(512, 1)
                 // per 2-query block (word 2 (i mod 2) + (j mod 2) of counter (j/2, i/2, h, b))
                 const int ibase = i0 + ib;
                 uint32_t kb = 0;
-                if ((ibase & 1) == 0) {
+                if ((ibase & 1) == 0 && (I0[I_KVBASE] & 1) == 0) {
+                  // keys 2m, 2m + 1 are lanes 2m, 2m + 1: each lane makes every other
+                  // call of the pair and hands its partner the two words it needs
+                  const uint32_t odd = lane & 1;
+#pragma unroll
+                  for (int m = 0; m < 8; ++m) {
+                    const uint4 rr = philox4x32_10(
+                        make_uint4(uint32_t(j) >> 1, uint32_t(ibase >> 1) + 2 * m + odd, hq, bseq), a.drop_k0,
+                        a.drop_k1);
+                    const uint32_t ev = uint32_t(rr.x >= a.drop_thresh) | (uint32_t(rr.z >= a.drop_thresh) << 1);
+                    const uint32_t od = uint32_t(rr.y >= a.drop_thresh) | (uint32_t(rr.w >= a.drop_thresh) << 1);
+                    const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? ev : od, 1);
+                    const uint32_t lo = odd ? got : ev, hi = odd ? od : got;  // query blocks 2m, 2m + 1
+                    kb |= (lo | (hi << 2)) << (4 * m);
+                  }
+                } else if ((ibase & 1) == 0) {
 #pragma unroll
                   for (int e2 = 0; e2 < 16; ++e2) {
                     const uint4 rr = philox4x32_10(

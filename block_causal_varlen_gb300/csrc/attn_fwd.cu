@@ -403,6 +403,35 @@ __global__ void __launch_bounds__(384, 1)
           const float2 cs = make_float2(a.scale_log2, a.scale_log2), cm = make_float2(-m_eff, -m_eff);
           float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
+          // dropout keep bits of the tile's 128 keys for this row, bit k of word k / 32
+          // (keys c0 + 2e, c0 + 2e + 1 form one 2-key block: c0 is a multiple of 128)
+          uint32_t kbits[4] = {0u, 0u, 0u, 0u};
+          if constexpr (DROP) {
+            const uint32_t T = a.drop_thresh, kb0 = uint32_t(c0) >> 1, rb = uint32_t(grow) >> 1;
+            if ((I[I_ROW0] & 1) == 0) {
+              // rows 2m, 2m + 1 are lanes 2m, 2m + 1: each lane makes every other call
+              // of the pair and hands its partner the two words the partner needs
+              const uint32_t odd = lane & 1;
+#pragma unroll 8
+              for (int m = 0; m < 32; ++m) {
+                const uint4 rr = philox4x32_10(make_uint4(kb0 + 2 * m + odd, rb, uint32_t(h), uint32_t(b)),
+                                               a.drop_k0, a.drop_k1);
+                const uint32_t ev = uint32_t(rr.x >= T) | (uint32_t(rr.y >= T) << 1);
+                const uint32_t od = uint32_t(rr.z >= T) | (uint32_t(rr.w >= T) << 1);
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? ev : od, 1);
+                const uint32_t lo = odd ? got : ev, hi = odd ? od : got;  // key blocks 2m, 2m + 1
+                kbits[m >> 3] |= (lo | (hi << 2)) << ((4 * m) & 31);
+              }
+            } else {
+#pragma unroll 8
+              for (int e = 0; e < 64; ++e) {
+                const uint4 rr = philox4x32_10(make_uint4(kb0 + e, rb, uint32_t(h), uint32_t(b)),
+                                               a.drop_k0, a.drop_k1);
+                const uint32_t u0 = (grow & 1) ? rr.z : rr.x, u1 = (grow & 1) ? rr.w : rr.y;
+                kbits[e >> 4] |= (uint32_t(u0 >= T) | (uint32_t(u1 >= T) << 1)) << ((2 * e) & 31);
+              }
+            }
+          }
           uint32_t pk[2][32];
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
@@ -411,13 +440,9 @@ __global__ void __launch_bounds__(384, 1)
             t.y = ex2(t.y);
             s4[e & 3] = fadd2(s4[e & 3], t);
             if constexpr (DROP) {
-              // keys c0 + 2e, c0 + 2e + 1 form one 2-key block (c0 is a multiple of 128);
-              // the row sum above keeps the undropped values, 1/(1-p) goes in the epilogue
-              const uint4 rr = philox4x32_10(make_uint4(uint32_t(c0 + 2 * e) >> 1, uint32_t(grow) >> 1,
-                                                        uint32_t(h), uint32_t(b)),
-                                             a.drop_k0, a.drop_k1);
-              const uint32_t u0 = (grow & 1) ? rr.z : rr.x, u1 = (grow & 1) ? rr.w : rr.y;
-              pk[e >> 5][e & 31] = pack_bf16(u0 >= a.drop_thresh ? t.x : 0.f, u1 >= a.drop_thresh ? t.y : 0.f);
+              // the row sum above keeps the undropped values; 1/(1-p) goes in the epilogue
+              const uint32_t kk = kbits[e >> 4] >> ((2 * e) & 31);
+              pk[e >> 5][e & 31] = pack_bf16((kk & 1) ? t.x : 0.f, (kk & 2) ? t.y : 0.f);
             } else {
               pk[e >> 5][e & 31] = pack_bf16(t.x, t.y);
             }
