@@ -695,6 +695,10 @@ int32_t bwd_common(const void* plan_host, const void* plan_dev, void* workspace,
   const PlanView& pv = c->pv;
   c->B = pv.hdr(H_B); c->C = pv.hdr(H_C); c->L = pv.hdr(H_L); c->H = pv.hdr(H_H); c->Hkv = pv.hdr(H_HKV);
   c->D = pv.hdr(H_D); c->Ck = pv.hdr(H_CK); c->nitems = pv.hdr(H_NITEMS); c->Lpad = pv.hdr(H_QTILES) * 128;
+  // the backward keeps dK and dV of a 128-key tile in TMEM next to the score and dP
+  // tiles: at head dim 256 those alone would need 768 of the 512 columns
+  if (c->D != 64 && c->D != 128)
+    return fail(BD_ERR_UNSUPPORTED, "the backward supports head dim 64 and 128; this plan has %d", c->D);
   c->ws = bwd_workspace_layout(c->nitems, c->H, c->Lpad);
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(BD_ERR_ALIGN, "workspace NULL or not 256-byte aligned");

@@ -54,10 +54,13 @@ struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16
   // K and V have rings of their own: a K tile is released as soon as both
   // slots' S MMAs have read it, so it can be refilled well ahead of its use.
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  // head dim 256: one query-head slot (its O takes TMEM columns 256..511) and
+  // single 64 KB K and V stages
+  static constexpr int kQSlots = (D == 256) ? 1 : 2;
+  static constexpr int kKStages = (D == 256) ? 1 : (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 256) ? 1 : (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffK = kOffQ + kQSlots * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
@@ -69,6 +72,8 @@ struct FwdCfg {
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
   static constexpr int kRegsLaunch = 168;  // 65536 / 384 threads, rounded down to 8
   static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
+  static_assert(kSmem <= 232448, "shared memory over the per-CTA limit");
+  static_assert(kOCol + kQSlots * D <= 512, "O accumulators exceed TMEM");
 };
 
 // barrier indices (8 bytes each)
@@ -597,10 +602,15 @@ extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, cons
   a.drop_k1 = uint32_t(pv.hdr(H_DROP_SEED_HI));
   const int32_t dbits = pv.hdr(H_DROP_SCALE_BITS);
   memcpy(&a.drop_scale, &dbits, 4);
+  if (D == 256 && a.slots != 1) return fail(BD_ERR_PLAN, "head dim 256 plans use one query head per CTA");
   if (a.drop_thresh != 0)
-    st = D == 128 ? launch_fwd<128, true>(mq, mk, mv, a, grid, s) : launch_fwd<64, true>(mq, mk, mv, a, grid, s);
+    st = D == 256   ? launch_fwd<256, true>(mq, mk, mv, a, grid, s)
+         : D == 128 ? launch_fwd<128, true>(mq, mk, mv, a, grid, s)
+                    : launch_fwd<64, true>(mq, mk, mv, a, grid, s);
   else
-    st = D == 128 ? launch_fwd<128, false>(mq, mk, mv, a, grid, s) : launch_fwd<64, false>(mq, mk, mv, a, grid, s);
+    st = D == 256   ? launch_fwd<256, false>(mq, mk, mv, a, grid, s)
+         : D == 128 ? launch_fwd<128, false>(mq, mk, mv, a, grid, s)
+                    : launch_fwd<64, false>(mq, mk, mv, a, grid, s);
   if (st) return st;
   return ok();
 }

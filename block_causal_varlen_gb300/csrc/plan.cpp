@@ -195,7 +195,8 @@ int32_t check_desc(const bd_plan_desc* d) {
   if (d->S % d->cp) return fail(BD_ERR_NOT_DIVISIBLE, "S = %d not a multiple of cp = %d", d->S, d->cp);
   if (d->H <= 0 || d->Hkv <= 0 || d->H % d->Hkv)
     return fail(BD_ERR_UNSUPPORTED, "H = %d must be a positive multiple of Hkv = %d", d->H, d->Hkv);
-  if (d->d != 64 && d->d != 128) return fail(BD_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", d->d);
+  if (d->d != 64 && d->d != 128 && d->d != 256)
+    return fail(BD_ERR_UNSUPPORTED, "head dim %d not in {64, 128, 256}", d->d);
   if (d->kv_mode != BD_KV_GATHER && d->kv_mode != BD_KV_WINDOW)
     return fail(BD_ERR_ARG, "kv_mode %d unknown", d->kv_mode);
   if (!d->cu_seqlens || !d->cu_offsets) return fail(BD_ERR_ARG, "cu_seqlens / cu_offsets NULL");
@@ -219,7 +220,9 @@ int32_t build(const bd_plan_desc* d, Built* out) {
   const int32_t C = d->nchunks, L = d->S / d->cp, G = d->H / d->Hkv;
   P.C = C;
   P.Ck = d->kv_mode == BD_KV_GATHER ? 1 : C;
-  P.slots = (G % 2 == 0) ? 2 : 1;
+  // two query heads of a GQA group share each K/V tile; at head dim 256 one head's
+  // O accumulator already takes half of TMEM, so a CTA serves a single head
+  P.slots = (d->d != 256 && G % 2 == 0) ? 2 : 1;
   P.qtiles = (L + kTile - 1) / kTile;
   P.nbuf = d->B * P.Ck;
   std::vector<bd_segment_t> tmp;

@@ -110,3 +110,11 @@ def test_same_seed_same_result_other_seed_differs():
     c = _run(wl, bd.BD_KV_GATHER, 0.3, 8)
     assert torch.equal(a[2], b[2]) and torch.equal(a[5], b[5])
     assert not torch.equal(a[2], c[2])
+
+
+def test_dropout_two_sequences():
+    """Two sequences in one batched launch: the sequence index is a counter word,
+    so each sequence gets its own mask."""
+    wl = dataclasses.replace(workloads.config(1), name="two_seqs_s512", B=2, cu=[[0, 200, 350, 512], [0, 100, 300]])
+    for mode in (bd.BD_KV_GATHER, bd.BD_KV_WINDOW):
+        _check(wl, mode, 0.25, SEED + 3)
