@@ -127,12 +127,18 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_digest(kernel):
-    """sha256 over the kernel's source files, in the listed order."""
+    """sha256 over the kernel's source files (in the listed order) with comments
+    and blank lines removed, so that only code changes make recorded counters stale."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "block_causal_varlen_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "block_causal_varlen_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -28,6 +28,9 @@
 //                reduce-adds (128 x 16 fp32 boxes staged through two shared
 //                memory buffers); at the end of a unit write dK (x scale) and dV.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV, dK after that.
+// The DROP instantiation regenerates the forward's dropout keep mask
+// (Philox4x32-10 from the plan's seed): dV reads the dropped, rescaled P^T and
+// dS = P (keep dP / (1 - p) - D) uses the undropped P.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -22,6 +22,11 @@
 // after that; P_s (bf16 pairs) overwrites the first 64 columns of S_s.
 // Online softmax works in the log2 domain and only rescales O when the row
 // maximum grows by more than 2^8 (exact: the final 1/l uses the same stale max).
+// Head dim 256 runs one slot per CTA (its O takes TMEM columns 256..511).
+// The DROP instantiation applies attention dropout to P before the PV product
+// with a Philox4x32-10 keep mask (Salmon et al., SC 2011) regenerated from the
+// plan's seed; the row sum keeps the undropped values and 1/(1-p) is applied
+// with 1/l in the epilogue.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
