@@ -39,5 +39,5 @@ from .attention import (  # noqa: F401
 )
 from .dropout import (  # noqa: F401
     philox4x32_10, keep_threshold, keep_mask, attention_fwd_dropout, attention_bwd_dropout,
-    chunk_fwd_dropout, chunk_bwd_dropout,
+    chunk_fwd_dropout, chunk_bwd_dropout, attention_rows_dropout, attention_bwd_cols_dropout,
 )

@@ -187,3 +187,78 @@ def chunk_bwd_dropout(q_chunk, k_buf, v_buf, do_chunk, cu, S, row_offset, p: flo
         dq[:, h] = scale * (ds @ k[:, g])
         dk[:, g] += scale * (ds.T @ q[:, h])
     return dq, dk, dv
+
+
+def _doc_extents(cu):
+    return [(int(cu[d]), int(cu[d + 1])) for d in range(len(cu) - 1) if cu[d + 1] > cu[d]]
+
+
+def attention_rows_dropout(q, k, v, do, cu, rows, p: float, seed: int, b: int = 0, scale=None,
+                           dtype=torch.float64):
+    """O [R, H, d], LSE [H, R] and dQ [R, H, d] with dropout for selected query
+    rows of a whole sequence. Each row needs only its own document's keys up to
+    itself, so rows are evaluated document by document."""
+    S, H, d = q.shape
+    G = _heads(H, k.shape[1])
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    rows = np.asarray(rows, dtype=np.int64)
+    o = torch.zeros(len(rows), H, d, dtype=dtype)
+    lse = torch.full((H, len(rows)), float("-inf"), dtype=dtype)
+    dq = torch.zeros(len(rows), H, d, dtype=dtype)
+    for a, e in _doc_extents(cu):
+        sel = np.flatnonzero((rows >= a) & (rows < e))
+        if len(sel) == 0:
+            continue
+        rr = rows[sel]
+        keys = np.arange(a, int(rr.max()) + 1)
+        mask = torch.from_numpy(keys[None, :] <= rr[:, None])
+        tr, tk = torch.from_numpy(rr), torch.from_numpy(keys)
+        qr, dor = q[tr].to(dtype), do[tr].to(dtype)           # only the slices used
+        kk, vk = k[tk].to(dtype), v[tk].to(dtype)
+        for h in range(H):
+            g = h // G
+            l_h, pr = _softmax_block(qr[:, h], kk[:, g], mask, scale)
+            z = _dropout_block(b, h, rr, keys, p, seed, dtype)
+            oh = (pr * z) @ vk[:, g]
+            dD = (dor[:, h] * oh).sum(-1)
+            ds = pr * (z * (dor[:, h] @ vk[:, g].T) - dD[:, None])
+            o[sel, h] = oh
+            lse[h, sel] = l_h
+            dq[sel, h] = scale * (ds @ kk[:, g])
+    return o, lse, dq
+
+
+def attention_bwd_cols_dropout(q, k, v, do, cu, cols, p: float, seed: int, b: int = 0, scale=None,
+                               dtype=torch.float64):
+    """dK, dV [len(cols), Hkv, d] with dropout for selected key columns of a whole
+    sequence, document by document: only the query rows of a column's document at
+    or after the document's earliest selected column are evaluated."""
+    S, H, d = q.shape
+    Hkv = k.shape[1]
+    G = _heads(H, Hkv)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    cols = np.asarray(cols, dtype=np.int64)
+    dk = torch.zeros(len(cols), Hkv, d, dtype=dtype)
+    dv = torch.zeros(len(cols), Hkv, d, dtype=dtype)
+    for a, e in _doc_extents(cu):
+        sel = np.flatnonzero((cols >= a) & (cols < e))
+        if len(sel) == 0:
+            continue
+        rr = np.arange(int(cols[sel].min()), e)
+        keys = np.arange(a, e)
+        mask = torch.from_numpy(keys[None, :] <= rr[:, None])
+        tr, tk = torch.from_numpy(rr), torch.from_numpy(keys)
+        cidx = torch.from_numpy(cols[sel] - a)
+        qr, dor = q[tr].to(dtype), do[tr].to(dtype)           # only the slices used
+        kk, vk = k[tk].to(dtype), v[tk].to(dtype)
+        for h in range(H):
+            g = h // G
+            _, pr = _softmax_block(qr[:, h], kk[:, g], mask, scale)
+            z = _dropout_block(b, h, rr, keys, p, seed, dtype)
+            oh = (pr * z) @ vk[:, g]
+            dD = (dor[:, h] * oh).sum(-1)
+            pc, zc = pr[:, cidx], z[:, cidx]
+            ds = pc * (zc * (dor[:, h] @ vk[cidx, g].T) - dD[:, None])
+            dv[sel, g] += (pc * zc).T @ dor[:, h]
+            dk[sel, g] += scale * (ds.T @ qr[:, h])
+    return dk, dv

@@ -168,3 +168,19 @@ def test_workload_shapes_run():
     q, k, v, do = workloads.tensors(wl)
     o, lse = oracle.chunk_fwd_dropout(q[0, :wl.L], k[0], v[0], wl.cu[0], wl.S, 0, 0.1, 42)
     assert torch.isfinite(o).all()
+
+
+def test_sampled_rows_and_columns_equal_the_full_oracle():
+    cu, S, H, Hkv, p, seed, b = [0, 10, 24, 30], 32, 4, 2, 0.35, 77, 1
+    q, k, v, do = _inputs(S, H, Hkv, 8, seed=4)
+    dq, dk, dv, o, lse = oracle.attention_bwd_dropout(q, k, v, do, cu, p, seed, b=b)
+    rows = [0, 5, 9, 10, 23, 29, 30, 31]
+    o_r, lse_r, dq_r = oracle.attention_rows_dropout(q, k, v, do, cu, rows, p, seed, b=b)
+    assert (o_r - o[rows]).abs().max() < 1e-12 and (dq_r - dq[rows]).abs().max() < 1e-12
+    ref = lse[:, rows]
+    assert torch.equal(torch.isneginf(lse_r), torch.isneginf(ref))
+    fin = torch.isfinite(ref)
+    assert (lse_r[fin] - ref[fin]).abs().max() < 1e-12
+    cols = [0, 3, 9, 12, 23, 24, 29, 31]
+    dk_c, dv_c = oracle.attention_bwd_cols_dropout(q, k, v, do, cu, cols, p, seed, b=b)
+    assert (dk_c - dk[cols]).abs().max() < 1e-12 and (dv_c - dv[cols]).abs().max() < 1e-12

@@ -118,3 +118,37 @@ def test_dropout_two_sequences():
     wl = dataclasses.replace(workloads.config(1), name="two_seqs_s512", B=2, cu=[[0, 200, 350, 512], [0, 100, 300]])
     for mode in (bd.BD_KV_GATHER, bd.BD_KV_WINDOW):
         _check(wl, mode, 0.25, SEED + 3)
+
+
+@pytest.mark.parametrize("i", [3, 4])
+def test_dropout_full_size_sampled(i):
+    """Full-size workloads in the launch configuration the benchmark times
+    (needed-only windows, owner sums): O, LSE and dQ on sampled rows, dK / dV on
+    sampled key columns, against the row / column dropout oracles."""
+    import numpy as np
+    wl = workloads.config(i)
+    mode, p, seed = bd.BD_KV_WINDOW, 0.1, SEED + 9
+    plan, (q, k, v, do), out, lse, dq, dkw, dvw = _run(wl, mode, p, seed)
+    # owner rows from the window partials (what bd_owner_sum computes in the step)
+    dk = torch.zeros(wl.B, 1, wl.S, wl.Hkv, wl.d, dtype=torch.float32, device="cuda")
+    dv = torch.zeros_like(dk)
+    bd.bd_owner_sum(plan, dkw.cuda(), dvw.cuda(), dk, dv)
+    torch.cuda.synchronize()
+    dk, dv = dk.view(wl.B, wl.S, wl.Hkv, wl.d).cpu(), dv.view(wl.B, wl.S, wl.Hkv, wl.d).cpu()
+    out = out.view(wl.B, wl.S, wl.H, wl.d)
+    lse = lse.permute(0, 2, 1, 3).reshape(wl.B, wl.H, wl.S)
+    dq = dq.view(wl.B, wl.S, wl.H, wl.d)
+    rng = np.random.default_rng(i)
+    b = 0
+    cu = wl.cu[b]
+    rows = gu.sample_rows(wl, b, n_rand=12 if i == 4 else 24)
+    o_r, l_r, dq_r = oracle.attention_rows_dropout(q[b], k[b], v[b], do[b], cu, rows, p, seed, b=b)
+    gu.o_check(out[b, rows].float(), o_r)
+    gu.lse_check(lse[b][:, rows], l_r)
+    assert gu.max_rel(dq[b, rows], dq_r) <= gu.GRAD_REL
+    # key columns near document ends (few attending rows): the last rows of each document
+    cols = sorted({e - 1 - t for e in cu[1:] for t in range(0, 6 if i == 4 else 3)} |
+                  {int(x) for x in rng.integers(max(0, cu[-1] - 64), cu[-1], size=4)})
+    dk_c, dv_c = oracle.attention_bwd_cols_dropout(q[b], k[b], v[b], do[b], cu, cols, p, seed, b=b)
+    assert gu.max_rel(dk[b, cols], dk_c) <= gu.GRAD_REL
+    assert gu.max_rel(dv[b, cols], dv_c) <= gu.GRAD_REL
