@@ -223,13 +223,15 @@ def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accu
                              _stream(stream)))
 
 
-def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None):
-    """First backward step only: D, log2 LSE, document starts; zeroes dq."""
+def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None, clear_dq=True):
+    """First backward step only: D, log2 LSE, document starts; zeroes dq unless
+    clear_dq is False (the caller then zeroes it before bd_attn_bwd_main)."""
     to, tg, tq = _tensor(out, "out"), _tensor(dout, "dout"), _tensor(dq, "dq")
     tl = _rowstat(lse, "lse")
-    check(load().bd_attn_bwd_pre(plan.host_ptr, plan.dev_ptr, C.byref(to), C.byref(tg), C.byref(tl), C.byref(tq),
-                                 C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
-                                 _stream(stream)))
+    check(load().bd_attn_bwd_pre_ex(plan.host_ptr, plan.dev_ptr, C.byref(to), C.byref(tg), C.byref(tl),
+                                    C.byref(tq), C.c_void_p(workspace.data_ptr()),
+                                    workspace.numel() * workspace.element_size(), int(bool(clear_dq)),
+                                    _stream(stream)))
 
 
 def bd_attn_bwd_main(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, accumulate_dkv=False, stream=None):

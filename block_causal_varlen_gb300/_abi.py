@@ -88,6 +88,9 @@ EXPORTS = {
     "bd_attn_bwd_pre": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                     C.POINTER(bd_rowstat), C.POINTER(bd_tensor), C.c_void_p, C.c_size_t,
                                     C.c_void_p]),
+    "bd_attn_bwd_pre_ex": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                       C.POINTER(bd_rowstat), C.POINTER(bd_tensor), C.c_void_p, C.c_size_t,
+                                       C.c_int32, C.c_void_p]),
     "bd_attn_bwd_main": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                      C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                      C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_int32, C.c_void_p,

@@ -711,9 +711,9 @@ int32_t bwd_common(const void* plan_host, const void* plan_dev, void* workspace,
 
 }  // namespace
 
-extern "C" int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, const bd_tensor* out,
-                                   const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+extern "C" int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_dev, const bd_tensor* out,
+                                      const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
+                                      size_t workspace_bytes, int32_t clear_dq, void* stream) {
   BwdCommon c;
   int32_t st = bwd_common(plan_host, plan_dev, workspace, workspace_bytes, &c);
   if (st) return st;
@@ -736,9 +736,15 @@ extern "C" int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, 
   p.rowds = reinterpret_cast<int32_t*>(wsb + c.ws.rowds);
   p.dq = static_cast<float*>(dq->ptr);
   p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
-  p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H;
+  p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H; p.clear_dq = clear_dq ? 1 : 0;
   if ((st = launch_bwd_pre(p, c.D, static_cast<cudaStream_t>(stream)))) return st;
   return ok();
+}
+
+extern "C" int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, const bd_tensor* out,
+                                   const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return bd_attn_bwd_pre_ex(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes, 1, stream);
 }
 
 extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, const bd_tensor* q,

@@ -31,7 +31,8 @@ BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
 }
 
 // One block per (item, row < Lpad): D for every head, the log2-domain LSE, the
-// row's document start, and zeroing of the row's dQ accumulator. Threads take
+// row's document start, and (unless the caller cleared it already) zeroing of the
+// row's dQ accumulator. Threads take
 // 16-byte pieces of O / dO (all heads of the row); a head's pieces sit in
 // consecutive lanes and are summed with shuffles.
 template <int D>
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
       a.lse2[sidx] = ds >= 0 ? lse * 1.4426950408889634f : inf;
     }
   }
+  if (!a.clear_dq) return;
   float* dqrow = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = tid; k < a.H * (D / 4); k += 256) {

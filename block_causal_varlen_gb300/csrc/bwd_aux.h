@@ -17,9 +17,9 @@ struct BwdPreArgs {
   float* lse2;     // workspace [nitems, H, Lpad]: LSE * log2(e), +inf on invalid rows
   float* dstat;    // workspace [nitems, H, Lpad]: D = <dO, O>
   int32_t* rowds;  // workspace [nitems, Lpad]: global start row of the row's document, INT_MAX if invalid
-  float* dq;       // zeroed
+  float* dq;       // zeroed when clear_dq is set
   int64_t q_sb, q_sc, q_sr, q_sh;
-  int32_t nitems, C, L, Lpad, H;
+  int32_t nitems, C, L, Lpad, H, clear_dq;
 };
 
 // Workspace layout of the backward (offsets in bytes, 256-byte aligned).

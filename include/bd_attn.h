@@ -255,6 +255,13 @@ BD_API int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, cons
                         const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* bd_attn_bwd_pre_ex -- bd_attn_bwd_pre with clear_dq = 0 leaving dq as it is:
+ * for callers that zero the fp32 dq accumulator themselves, e.g. on another
+ * stream while the forward runs (dq must be zero before bd_attn_bwd_main). */
+BD_API int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_dev, const bd_tensor* out,
+                           const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
+                           size_t workspace_bytes, int32_t clear_dq, void* stream);
+
 /* bd_attn_bwd_main -- the second step of bd_attn_bwd on its own: dq (added
  * into what bd_attn_bwd_pre zeroed), dk and dv from the workspace that
  * bd_attn_bwd_pre filled for the same plan and tensors. */

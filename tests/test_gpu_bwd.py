@@ -227,3 +227,30 @@ def test_claim_counters_reset_between_launches():
     (dq1, dk1, dv1), (dq2, dk2, dv2) = grads
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # dK/dV accumulate in TMEM: deterministic
     assert gu.max_rel(dq2, dq1) < 1e-5                        # dQ adds in arrival order
+
+
+def test_pre_without_clearing_after_caller_zeroes_dq():
+    """bd_attn_bwd_pre_ex with clear_dq = 0 and a dq the caller zeroed on another
+    stream gives the gradients of the clearing form."""
+    wl = workloads.config(2)
+    q, k, v, do = workloads.tensors(wl)
+    plan, out, lse, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, bd.BD_KV_GATHER)
+    dod = gu.as_chunks(do.cuda(), wl.cp)
+    ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
+    res = []
+    for clear in (True, False):
+        dq = torch.full(qd.shape, float("nan"), dtype=torch.float32, device="cuda")
+        if not clear:
+            side = torch.cuda.Stream()
+            with torch.cuda.stream(side):
+                dq.zero_()
+            torch.cuda.current_stream().wait_stream(side)
+        dk = torch.zeros(kd.shape, dtype=torch.float32, device="cuda")
+        dv = torch.zeros_like(dk)
+        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, ws, clear_dq=clear)
+        bd.bd_attn_bwd_main(plan, qd, kd, vd, dod, dq, dk, dv, ws)
+        torch.cuda.synchronize()
+        res.append((dq.cpu(), dk.cpu(), dv.cpu()))
+    (dq1, dk1, dv1), (dq2, dk2, dv2) = res
+    assert torch.isfinite(dq2).all() and gu.max_rel(dq2, dq1) < 1e-5
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
