@@ -158,6 +158,21 @@ def kernel_traffic(kernel, workload):
     return None
 
 
+def tile_stats(plan, wl):
+    """128 x 128 (query, key) tiles per head: those the kernels visit (tiles that
+    are fully masked are never loaded) against the dense causal tiles of every chunk."""
+    import math
+    per_head = plan.fwd_tiles() * plan.slots() / wl.H  # a forward work unit serves slots() heads
+    qt = math.ceil(wl.L / 128)
+    dense = 0
+    for c in range(wl.cp):         # causal: chunk c's query tiles against keys [0, (c+1) L)
+        for t in range(qt):
+            dense += math.ceil(min(wl.S, c * wl.L + (t + 1) * 128) / 128)
+    dense *= wl.B
+    return {"visited_per_head": per_head, "dense_causal_per_head": dense,
+            "skipped_fraction": 1.0 - per_head / dense if dense else 0.0}
+
+
 def useful_flops(plan, wl):
     n = plan.useful_pairs() * wl.H
     return n, 4.0 * wl.d * n, 10.0 * wl.d * n
@@ -467,6 +482,7 @@ def run_ours(args):
                        "Hkv": wl.Hkv, "d": wl.d, "kv_mode": wl.kv_mode, "layout_seed": wl.seed,
                        "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
                        "dropout": args.dropout,
+                       "tiles": tile_stats(plan, wl),
                        "l2": "flushed between steps by a 256 MiB write outside the step events"},
             "fwd_tflops": f_fwd / (t_fwd * 1e-3) / 1e12,
             "bwd_tflops": f_bwd / ((t_pre + t_main + t_own) * 1e-3) / 1e12,

@@ -145,7 +145,11 @@ class Plan:
         return int(self.host[field])
 
     # index of a few header words (see csrc/plan_layout.h)
-    H_NFWD, H_NBWD, H_KV_ROWS, H_FWD_TILES_LO, H_FWD_TILES_HI = 18, 20, 22, 29, 30
+    H_NFWD, H_NBWD, H_KV_ROWS, H_SLOTS, H_FWD_TILES_LO, H_FWD_TILES_HI = 18, 20, 22, 24, 29, 30
+
+    def slots(self) -> int:
+        """Query heads per forward work unit (2 when GQA heads are paired, else 1)."""
+        return int(self.host[self.H_SLOTS])
 
     def fwd_tiles(self) -> int:
         """Key tiles visited by the forward over all work units (each for `slots` heads)."""
