@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   const int item = blockIdx.x / a.Lpad, l = blockIdx.x % a.Lpad;
   const int b = item / a.C, c = item % a.C;
   const int tid = threadIdx.x;
-  constexpr int CPH = D / 8;  // 16-byte pieces per head (8 or 16: groups never straddle a warp)
+  constexpr int CPH = D / 8;  // 16-byte pieces per head (8, 16 or 32: groups never straddle a warp)
   const float inf = __int_as_float(0x7f800000);
   if (l >= a.L) {
     for (int h = tid; h < a.H; h += blockDim.x) {
@@ -101,7 +101,8 @@ int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
   const int64_t blocks = int64_t(a.nitems) * a.Lpad;
   if (blocks == 0) return BD_OK;
   if (blocks > 0x7fffffff) return fail(BD_ERR_UNSUPPORTED, "too many rows for the statistics kernel");
-  if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);
+  if (D == 256) bd_bwd_pre_kernel<256><<<unsigned(blocks), 256, 0, s>>>(a);
+  else if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);
   else bd_bwd_pre_kernel<64><<<unsigned(blocks), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? BD_OK : cuda_fail(e, "bd_bwd_pre_kernel launch");

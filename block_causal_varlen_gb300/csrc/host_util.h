@@ -16,9 +16,9 @@ int32_t check_tensor(const bd_tensor* t, const char* name, int elem_bytes, int64
                      int64_t H, bool need_tma);
 
 // Encodes a 5-D tiled TMA map over bf16 [B, C, rows, heads, d] with a box of
-// 128 rows x 64 columns of one head, 128-byte swizzle, zero fill out of bounds.
+// box_rows rows x 64 columns of one head, 128-byte swizzle, zero fill out of bounds.
 int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads,
-                       int64_t d, const char* name);
+                       int64_t d, const char* name, int box_rows = 128);
 
 // Encodes a 5-D tiled TMA map over fp32 [B, C, rows, heads, d] with a box of
 // 128 rows x 16 columns of one head, 64-byte swizzle (for reduce-adds).

@@ -312,6 +312,7 @@ int32_t build(const bd_plan_desc* d, Built* out) {
     const int32_t* cu = d->cu_seqlens + d->cu_offsets[b];
     const int32_t nd = d->cu_offsets[b + 1] - d->cu_offsets[b] - 1;
     const int32_t ntiles = (rows + kTile - 1) / kTile;
+    const int32_t qstep = bwd_query_step(d->d);
     for (int32_t kt = 0; kt < ntiles; ++kt) {
       const int32_t c0 = kv_base + kt * kTile;
       const int32_t last = std::min(std::min(c0 + kTile, kv_base + rows), svalid) - 1;
@@ -324,7 +325,7 @@ int32_t build(const bd_plan_desc* d, Built* out) {
         for (int32_t it = it_lo; it < it_hi; ++it) {
           const int32_t* I = &P.items[size_t(it) * kItemWords];
           const int32_t lo = std::max(c0, I[I_ROW0]), hi = std::min(q_end, I[I_ROW0] + L);
-          if (lo < hi) nq += (hi - 1 - I[I_ROW0]) / kTile - (lo - I[I_ROW0]) / kTile + 1;
+          if (lo < hi) nq += (hi - 1 - I[I_ROW0]) / qstep - (lo - I[I_ROW0]) / qstep + 1;
         }
       }
       for (int32_t g = 0; g < d->Hkv; ++g) {

@@ -53,7 +53,14 @@ enum : int { F_ITEM = 0, F_QTILE, F_H0, F_KTLO, F_NT, F_PAD0, F_PAD1, F_PAD2, kF
 // [128*kt, 128*kt+128)) for one K/V head, visiting the query tiles of chunk
 // items [item_lo, item_hi) that hold global rows in [q_lo, q_hi): the rows
 // that attend to at least one key of the tile (q_lo = q_hi when none).
+// nq counts (query step, query head) pairs; a query step is
+// bwd_query_step(d) rows of one chunk.
 enum : int { W_BUF = 0, W_KTILE, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_QLO, W_QHI, kBwdWords = 8 };
+
+// Query rows per backward step: 128, and 64 at head dim 256, where a 128-row Q
+// tile and dO tile (64 KB each) would not fit in shared memory next to the
+// resident K and V tiles.
+constexpr int bwd_query_step(int d) { return d == 256 ? 64 : kTile; }
 
 // device failure codes stored at H_STATUS
 enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };

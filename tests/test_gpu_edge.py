@@ -39,7 +39,7 @@ def _gpu():
     bd.load()
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("name", sorted(LAYOUTS))
 def test_edge_layout_fwd_bwd(name, mode, d):
