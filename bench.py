@@ -240,7 +240,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     torch.set_num_threads(len(os.sched_getaffinity(0)))
-    wl = workloads.config(args.workload)
+    wl = bench_workload(args)
     q, k, v, do = workloads.tensors(wl)
     chunks_all = [(b, c) for b in range(wl.B) for c in range(wl.cp) if wl.cu[b][-1] > c * wl.L]
     times, pairs = [], []
@@ -264,6 +264,17 @@ def run_reference(args):
     return 0
 
 
+def bench_workload(args):
+    """The workload `--workload` names, with `--head-dim` replacing its head dim."""
+    import dataclasses
+
+    import workloads
+    wl = workloads.config(args.workload)
+    if args.head_dim and args.head_dim != wl.d:
+        wl = dataclasses.replace(wl, d=args.head_dim, name=wl.name.replace(f"_d{wl.d}", f"_d{args.head_dim}"))
+    return wl
+
+
 # ------------------------------------------------------------------ our path
 
 def run_ours(args):
@@ -284,7 +295,7 @@ def run_ours(args):
     bdbuild.build()
     bd.load()
 
-    wl = workloads.config(args.workload)
+    wl = bench_workload(args)
     mode = bd.BD_KV_WINDOW if wl.kv_mode == "window" else bd.BD_KV_GATHER
     q, k, v, do = workloads.tensors(wl)
     plan = bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode)
@@ -517,6 +528,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="attention dropout probability (default 0, as in every benchmarked configuration)")
+    ap.add_argument("--head-dim", type=int, default=0, choices=[0, 64, 128, 256],
+                    help="replace the workload's head dim (default: keep it)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -72,8 +72,8 @@ struct BwdCfg {
   static constexpr int kPasses = D == 256 ? 2 : 1;
   static constexpr int kDH = D / kPasses;               // dK / dV / dQ columns per pass
   static constexpr int kQStages = D == 256 ? 1 : 2;     // Q tiles in flight
-  // head dim 256 forms dQ^T = K^T dS^T (lane = column of d) and adds it to global
-  // memory with red.global, which needs no staging buffer
+  // head dim 256 forms dQ^T = K^T dS^T (lane = column of d); each dQ warp
+  // transposes its 32 columns through two 16-row x 128-byte staging buffers
   static constexpr bool kDqT = D == 256;
   static constexpr int kTileBytes = 128 * D * 2;        // one K or V tile
   static constexpr int kQBox = kQRows * 128;            // one 64-column box of a Q / dO tile
@@ -84,11 +84,13 @@ struct BwdCfg {
   static constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;
   static constexpr int kOffDS = kOffDO + kQTileBytes;   // dS^T, 128 keys x kQRows queries bf16
   static constexpr int kDSBytes = 128 * kQRows * 2;
-  static constexpr int kOffStat = kOffDS + kDSBytes;    // per stage: lse2, D, ds of kQRows rows
-  static constexpr int kStatBytes = 3 * kQRows * 4;
-  static constexpr int kOffStage = kOffStat + kQStages * kStatBytes;  // dQ staging, two 128 rows x 64 bytes buffers
-  static constexpr int kStageBytes = kDqT ? 0 : 16384;
-  static constexpr int kOffBar = kOffStage + kStageBytes;
+  // dQ staging: two 128 rows x 64 bytes buffers, or (dQ^T) two 16 rows x 128 bytes
+  // buffers per dQ warp; 1024-byte aligned for the swizzle
+  static constexpr int kStatBytes = 3 * kQRows * 4;     // per stage: lse2, D, ds of kQRows rows
+  static constexpr int kStageBytes = 16384;
+  static constexpr int kOffStat = kDqT ? kOffDS + kDSBytes + kStageBytes : kOffDS + kDSBytes;
+  static constexpr int kOffStage = kDqT ? kOffDS + kDSBytes : kOffStat + kQStages * kStatBytes;
+  static constexpr int kOffBar = kDqT ? kOffStat + kQStages * kStatBytes : kOffStage + kStageBytes;
   static constexpr int kSmem = kOffBar + 256 + 1024;
   // TMEM columns: S^T / P^T [0, kQRows), dP^T after it, dQ (sharing dP^T's
   // columns, or its own for dQ^T), dV and dK from 256
@@ -107,7 +109,9 @@ struct BwdCfg {
 
 enum : int {
   C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_DOFULL, C_DOEMPTY, C_SFULL, C_DPFULL,
-  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_DVFREE, C_DKFREE, C_DRAIN, C_UFULL,
+  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_DVFREE, C_DKFREE, C_DRAIN,
+  C_DSFREE,  // head dim 256: dS^T of the step read by its last MMA (dQ^T)
+  C_UFULL,
   C_UEMPTY = C_UFULL + kUnitSlots, C_COUNT = C_UEMPTY + kUnitSlots
 };
 // warps that read each claimed unit from the ring: MMA thread, 8 P/dS warps, 4 dQ warps
@@ -400,19 +404,23 @@ __global__ void __launch_bounds__(512, 1)
                         (s > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar(C_DOEMPTY));
             if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
-            if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
             if (s == 0 && !(ok = mbar_wait(bar(C_DKFREE), (ua & 1) ^ 1, abort_flag))) break;
+            tc_fence_after();
+            // dK first: it is the last reader of the Q stage, whose next tile then
+            // loads while dQ^T runs
+#pragma unroll
+            for (int kk = 0; kk < QR / 16; ++kk)
+              mma_ss_lo(tmem + Cfg::kColDK, dDS_k + 2 * kk, dQe_mn + mnstep(kk), idAcc, (s > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar(C_QEMPTY0));
+            if (s == nsteps - 1) tc_commit(bar(C_ACCDONE));
+            if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ss_lo(tmem + Cfg::kColDQ, dKe_mn + mnstep(kk), dDS_mn + mnstep(kk), idDQ, kk > 0);
             tc_commit(bar(C_DQFULL));
-#pragma unroll
-            for (int kk = 0; kk < QR / 16; ++kk)
-              mma_ss_lo(tmem + Cfg::kColDK, dDS_k + 2 * kk, dQe_mn + mnstep(kk), idAcc, (s > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C_QEMPTY0));  // Q and dS^T of this step are free after dQ and dK
+            tc_commit(bar(C_DSFREE));
             if (s == nsteps - 1) {
-              tc_commit(bar(C_ACCDONE));
               if (e == 1) tc_commit(bar(C_KVEMPTY));
             } else {
               issue_s(sc + 1);
@@ -556,8 +564,10 @@ __global__ void __launch_bounds__(512, 1)
             if (threadIdx.x == 128) BD_TRACE_EVENT(13, int(sc));  // compute: dP ready
             tc_fence_after();
             // dS^T of the previous step must have been consumed by its dQ and dK MMAs
-            // (dK is the later one; its commit also releases that step's Q stage)
-            if (sc > 0 && !(ok = mbar_wait(bar(C_QEMPTY0 + ((sc - 1) % QS)), ((sc - 1) / QS) & 1, abort_flag)))
+            // (the later of the two commits the stage's QEMPTY, or DSFREE for dQ^T)
+            if (sc > 0 && !(ok = Cfg::kDqT ? mbar_wait(bar(C_DSFREE), (sc - 1) & 1, abort_flag)
+                                           : mbar_wait(bar(C_QEMPTY0 + ((sc - 1) % QS)), ((sc - 1) / QS) & 1,
+                                                       abort_flag)))
               break;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
@@ -648,9 +658,11 @@ __global__ void __launch_bounds__(512, 1)
               if (!ok) break;
               tc_fence_after();
               if constexpr (Cfg::kDqT) {
-                // dQ^T of this pass's columns: lane rl holds column 128 pass + rl of
-                // the step's QR query rows; a warp's 32 lanes add 128 contiguous bytes
-                // of one row at a time
+                // dQ^T of this pass's columns: lane rl holds column 128 pass + rl of the
+                // step's QR query rows. Each warp turns its 32 columns into row-major
+                // 16-row x 32-column boxes (128-byte rows, 128-byte swizzle: 16-byte
+                // chunk c of row q sits at c ^ (q & 7)) in two buffers of its own and
+                // sends each with a TMA reduce-add (rows past L are clipped by the map)
                 constexpr int QR = Cfg::kQRows;
                 uint32_t r[QR / 32][32];
 #pragma unroll
@@ -660,12 +672,24 @@ __global__ void __launch_bounds__(512, 1)
                 for (int q = 0; q < QR / 32; ++q) reg_fence(r[q]);
                 tc_fence_before();
                 mbar_arrive(bar(C_DQEMPTY));
-                float* col = a.dq + b * a.q_sb + c * a.q_sc + int64_t(h) * a.q_sh + pass * Cfg::kDH + rl;
-                const int nrow = min(QR, a.L - t * QR);  // rows past the chunk are not stored
 #pragma unroll
-                for (int q = 0; q < QR; ++q)
-                  if (q < nrow)
-                    atomicAdd(col + int64_t(t * QR + q) * a.q_sr, __uint_as_float(r[q >> 5][q & 31]) * a.scale);
+                for (int rr = 0; rr < QR / 16; ++rr) {
+                  const uint32_t buf = sStage + (quarter * 2 + (rr & 1)) * 2048;
+                  if (lane == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
+                  __syncwarp();
+#pragma unroll
+                  for (int q = 0; q < 16; ++q) {
+                    const int row = rr * 16 + q;
+                    st_shared_f32(buf + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4,
+                                  __uint_as_float(r[row >> 5][row & 31]) * a.scale);
+                  }
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (lane == 0) {
+                    tma_reduce_add_5d(&tm_dq, buf, pass * Cfg::kDH + quarter * 32, h, t * QR + rr * 16, c, b);
+                    bulk_commit();
+                  }
+                }
               } else {
                 // dQ tile (128 query rows x D fp32) goes to global memory as TMA
                 // reduce-adds (rows past L are clipped by the map); the whole dQ row
@@ -744,7 +768,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (!ok) break;
     }
-    if (rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
+    if (Cfg::kDqT ? lane == 0 : rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
   }
 
   tc_fence_before();
@@ -901,7 +925,11 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
   if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if ((st = make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq"))) return st;
+  // dQ reduce boxes: 128 rows x 16 columns (64-byte swizzle), or at head dim 256
+  // (transposed dQ) 16 rows x 32 columns (128-byte swizzle)
+  if ((st = c.D == 256 ? make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 16)
+                       : make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq")))
+    return st;
   // Q / dO boxes are one backward query step high
   if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q", bwd_query_step(c.D)))) return st;
   if ((st = make_tmap_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout", bwd_query_step(c.D)))) return st;

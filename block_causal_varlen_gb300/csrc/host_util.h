@@ -21,9 +21,10 @@ int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t 
                        int64_t d, const char* name, int box_rows = 128);
 
 // Encodes a 5-D tiled TMA map over fp32 [B, C, rows, heads, d] with a box of
-// 128 rows x 16 columns of one head, 64-byte swizzle (for reduce-adds).
+// box_rows rows x box_cols columns of one head (for reduce-adds): 16 columns take
+// the 64-byte swizzle, 32 columns the 128-byte swizzle.
 int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
-                             const char* name);
+                             const char* name, int box_cols = 16, int box_rows = 128);
 
 // Number of SMs of the current device (cached per device).
 int32_t sm_count(int* out);
