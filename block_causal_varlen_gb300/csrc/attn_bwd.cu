@@ -1,4 +1,5 @@
-// Backward of block-causal varlen chunked attention on sm_103a.
+// Backward of block-causal varlen chunked attention on sm_103a, head dim 64 and
+// 128 (head dim 256 has its own kernel in attn_bwd256.cu).
 //
 // What it computes, for the loss sum(O * dO) (the analytic gradient of the
 // forward of the NeMo Automodel page "block-diagonal varlen CP for packed
@@ -37,6 +38,7 @@
 #include <cstring>
 
 #include "bwd_aux.h"
+#include "bwd_kernel.cuh"
 #include "host_util.h"
 #include "plan_layout.h"
 #include "ptx.cuh"
@@ -44,96 +46,36 @@
 namespace bd {
 using namespace dev;
 
-struct BwdArgs {
-  const int32_t* plan;
-  const float* lse2;
-  const float* dstat;
-  const int32_t* rowds;
-  float* dq;
-  int64_t q_sb, q_sc, q_sr, q_sh;
-  float* dk;
-  int64_t k_sb, k_sc, k_sr, k_sh;
-  float* dv;
-  int64_t v_sb, v_sc, v_sr, v_sh;
-  int32_t L, Lpad, H, G, Ck, n_work, accumulate, dk_rows;
-  float scale, scale_log2;
-  // attention dropout (used by the DROP instantiation): keep iff Philox word >= thresh
-  uint32_t drop_thresh, drop_k0, drop_k1;
-  float drop_scale;
-};
-
 template <int D>
 struct BwdCfg {
-  // Query rows per step and passes over column halves of dK / dV / dQ. Head dim
-  // 256 takes 64-row steps and two passes of 128 columns: S^T and dP^T are
-  // recomputed in each pass (they contract over all of d), while each pass keeps
-  // only its half of dV and dK in TMEM (both halves would take 512 columns).
-  static constexpr int kQRows = bwd_query_step(D);
-  static constexpr int kPasses = D == 256 ? 2 : 1;
-  static constexpr int kDH = D / kPasses;               // dK / dV / dQ columns per pass
-  static constexpr int kQStages = D == 256 ? 1 : 2;     // Q tiles in flight
-  // head dim 256 forms dQ^T = K^T dS^T (lane = column of d); each dQ warp
-  // transposes its 32 columns through two 16-row x 128-byte staging buffers
-  static constexpr bool kDqT = D == 256;
-  static constexpr int kTileBytes = 128 * D * 2;        // one K or V tile
-  static constexpr int kQBox = kQRows * 128;            // one 64-column box of a Q / dO tile
-  static constexpr int kQTileBytes = kQRows * D * 2;
+  static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
-  static constexpr int kOffQ = 2 * kTileBytes;
-  static constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;
-  static constexpr int kOffDS = kOffDO + kQTileBytes;   // dS^T, 128 keys x kQRows queries bf16
-  static constexpr int kDSBytes = 128 * kQRows * 2;
-  // dQ staging: two 128 rows x 64 bytes buffers, or (dQ^T) two 16 rows x 128 bytes
-  // buffers per dQ warp; 1024-byte aligned for the swizzle
-  static constexpr int kStatBytes = 3 * kQRows * 4;     // per stage: lse2, D, ds of kQRows rows
-  static constexpr int kStageBytes = 16384;
-  static constexpr int kOffStat = kDqT ? kOffDS + kDSBytes + kStageBytes : kOffDS + kDSBytes;
-  static constexpr int kOffStage = kDqT ? kOffDS + kDSBytes : kOffStat + kQStages * kStatBytes;
-  static constexpr int kOffBar = kDqT ? kOffStat + kQStages * kStatBytes : kOffStage + kStageBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;          // two stages
+  static constexpr int kOffDO = 4 * kTileBytes;
+  static constexpr int kOffDS = 5 * kTileBytes;         // dS^T, 128 keys x 128 queries bf16
+  static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128], ds[128]
+  static constexpr int kStatBytes = 3 * 512;
+  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;  // dQ staging, two 128 rows x 64 bytes buffers
+  static constexpr int kOffBar = kOffStage + 16384;
   static constexpr int kSmem = kOffBar + 256 + 1024;
-  // TMEM columns: S^T / P^T [0, kQRows), dP^T after it, dQ (sharing dP^T's
-  // columns, or its own for dQ^T), dV and dK from 256
-  static constexpr int kColDP = kQRows;
-  static constexpr int kColDQ = kDqT ? 2 * kQRows : kColDP;
-  static constexpr int kColDV = 256, kColDK = 256 + kDH;
+  static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
   static constexpr int kRegsCtl = 96, kRegsCompute = 120, kRegsDq = 176;
   static constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsCompute + 128 * kRegsDq;
   static constexpr int kRegsLaunch = 128;  // 65536 / 512 threads: what ptxas assigns at launch
   static_assert(kRegsNeeded <= kRegsLaunch * kThreads, "register split exceeds the launch's registers");
-  static_assert(kSmem <= 232448, "shared memory beyond the 227 KB a CTA may have");
-  static_assert(kColDK + kDH <= 512 && kColDQ + (kDqT ? kQRows : kDH) <= kColDV, "TMEM columns overlap");
 };
 
 enum : int {
   C_KVFULL = 0, C_KVEMPTY, C_QFULL0, C_QFULL1, C_QEMPTY0, C_QEMPTY1, C_DOFULL, C_DOEMPTY, C_SFULL, C_DPFULL,
-  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_DVFREE, C_DKFREE, C_DRAIN,
-  C_DSFREE,  // head dim 256: dS^T of the step read by its last MMA (dQ^T)
-  C_UFULL,
+  C_PREADY, C_DSREADY, C_DQFULL, C_DQEMPTY, C_ACCDONE, C_DVFREE, C_DKFREE, C_DRAIN, C_UFULL,
   C_UEMPTY = C_UFULL + kUnitSlots, C_COUNT = C_UEMPTY + kUnitSlots
 };
 // warps that read each claimed unit from the ring: MMA thread, 8 P/dS warps, 4 dQ warps
 constexpr uint32_t kUnitConsumers = 1 + 8 + 4;
 static_assert(8 * C_COUNT + 16 + 4 * kUnitSlots <= 256, "barriers, TMEM slot, abort flag and unit ring overflow their region");
-
-// Iterates the (item, query step, head) steps of a backward work unit in the
-// same order for every role; a query step is QR rows of one chunk.
-template <int QR>
-struct StepRange {
-  const int32_t* items;
-  int it_lo, it_hi, q_lo, q_hi, L;
-  __device__ bool tiles(int it, int& t0, int& t1, int& r0) const {
-    const int32_t* I = items + it * kItemWords;
-    r0 = I[I_ROW0];
-    const int lo = max(q_lo, r0), hi = min(q_hi, r0 + L);
-    if (lo >= hi) return false;
-    t0 = (lo - r0) / QR;
-    t1 = (hi - 1 - r0) / QR;
-    return true;
-  }
-};
 
 template <int D, bool DROP>
 __global__ void __launch_bounds__(512, 1)
@@ -205,63 +147,59 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_5d(sV + hf * 16384, &tm_v, bar(C_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
         }
         ++u;
-        const StepRange<Cfg::kQRows> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+        const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
         // Q / dO / row statistics of a step are loaded once its stage is free, which
         // is late (the stage's previous Q is read by the last MMA of the step before);
         // so each step's tiles are first prefetched into L2 one step ahead
         struct Step { int it, t, h, b, c; };
         Step prev{};
         bool have_prev = false;
-        constexpr int QR = Cfg::kQRows, QS = Cfg::kQStages;
         auto load_step = [&](const Step& x) {
-          const int qs = sc % QS;
-          if (!(ok = mbar_wait(bar(C_QEMPTY0 + qs), ((sc / QS) & 1) ^ 1, abort_flag))) return;
-          mbar_expect_tx(bar(C_QFULL0 + qs), Cfg::kQTileBytes + Cfg::kStatBytes);
+          const int qs = sc & 1;
+          if (!(ok = mbar_wait(bar(C_QEMPTY0 + qs), ((sc >> 1) & 1) ^ 1, abort_flag))) return;
+          mbar_expect_tx(bar(C_QFULL0 + qs), Cfg::kTileBytes + Cfg::kStatBytes);
           for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_5d(sQ + qs * Cfg::kQTileBytes + hf * Cfg::kQBox, &tm_q, bar(C_QFULL0 + qs), hf * 64, x.h,
-                        x.t * QR, x.c, x.b);
+            tma_load_5d(sQ + qs * Cfg::kTileBytes + hf * 16384, &tm_q, bar(C_QFULL0 + qs), hf * 64, x.h, x.t * 128,
+                        x.c, x.b);
           const uint32_t st = sbase + Cfg::kOffStat + qs * Cfg::kStatBytes;
-          const int64_t srow = (int64_t(x.it) * a.H + x.h) * a.Lpad + x.t * QR;
-          bulk_load(st, a.lse2 + srow, QR * 4, bar(C_QFULL0 + qs));
-          bulk_load(st + QR * 4, a.dstat + srow, QR * 4, bar(C_QFULL0 + qs));
-          bulk_load(st + 2 * QR * 4, a.rowds + int64_t(x.it) * a.Lpad + x.t * QR, QR * 4, bar(C_QFULL0 + qs));
+          const int64_t srow = (int64_t(x.it) * a.H + x.h) * a.Lpad + x.t * 128;
+          bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
+          bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
+          bulk_load(st + 1024, a.rowds + int64_t(x.it) * a.Lpad + x.t * 128, 512, bar(C_QFULL0 + qs));
           ++q_iss;
           if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) return;
-          mbar_expect_tx(bar(C_DOFULL), Cfg::kQTileBytes);
+          mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
           for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_5d(sDO + hf * Cfg::kQBox, &tm_do, bar(C_DOFULL), hf * 64, x.h, x.t * QR, x.c, x.b);
+            tma_load_5d(sDO + hf * 16384, &tm_do, bar(C_DOFULL), hf * 64, x.h, x.t * 128, x.c, x.b);
           ++do_iss;
           ++sc;
         };
-        // every pass over the unit's steps reloads their Q / dO tiles
-        for (int e = 0; e < Cfg::kPasses && ok; ++e)
-          for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
-            int t0, t1, r0;
-            if (!R.tiles(it, t0, t1, r0)) continue;
-            const int32_t* I = items + it * kItemWords;
-            const int b = I[I_B], c = I[I_C];
-            for (int t = t0; t <= t1 && ok; ++t)
-              for (int hh = 0; hh < a.G && ok; ++hh) {
-                const Step x{it, t, g * a.G + hh, b, c};
-                if (have_prev) load_step(prev);
-                prev = x;
-                have_prev = true;
-              }
-          }
+        for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+          int t0, t1, r0;
+          if (!R.tiles(it, t0, t1, r0)) continue;
+          const int32_t* I = items + it * kItemWords;
+          const int b = I[I_B], c = I[I_C];
+          for (int t = t0; t <= t1 && ok; ++t)
+            for (int hh = 0; hh < a.G && ok; ++hh) {
+              const Step x{it, t, g * a.G + hh, b, c};
+              if (have_prev) load_step(prev);
+              prev = x;
+              have_prev = true;
+            }
+        }
         if (have_prev && ok) load_step(prev);
       }
       if (!ok) {
         // wait for copies already issued before the shared memory goes away
         if (u > 0) mbar_wait_drain(bar(C_KVFULL), (u - 1) & 1);
-        constexpr uint32_t QS = Cfg::kQStages;
-        for (uint32_t x = (q_iss > QS ? q_iss - QS : 0); x < q_iss; ++x)
-          mbar_wait_drain(bar(C_QFULL0 + (x % QS)), (x / QS) & 1);
+        for (uint32_t x = (q_iss > 2 ? q_iss - 2 : 0); x < q_iss; ++x)
+          mbar_wait_drain(bar(C_QFULL0 + (x & 1)), (x >> 1) & 1);
         if (do_iss > 0) mbar_wait_drain(bar(C_DOFULL), (do_iss - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (Cfg::kPasses == 1 && lane == 0) {
+    if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idKM = idesc_bf16(128, D, false, true);   // A K-major, B MN-major
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);    // both MN-major
@@ -351,89 +289,6 @@ __global__ void __launch_bounds__(512, 1)
         tc_commit(bar(C_DRAIN));
         mbar_wait_drain(bar(C_DRAIN), 0);
       }
-    } else if (Cfg::kPasses == 2 && lane == 0) {
-      // head dim 256: 64-query steps, each unit walked twice (pass e accumulates
-      // columns [128 e, 128 e + 128) of dV and dK and adds the same columns of dQ)
-      constexpr int QR = Cfg::kQRows;
-      constexpr uint32_t idS = idesc_bf16(128, QR, false, false);       // S^T, dP^T: N = query rows
-      constexpr uint32_t idAcc = idesc_bf16(128, Cfg::kDH, false, true);  // dV, dK: B MN-major
-      constexpr uint32_t idDQ = idesc_bf16(128, QR, true, true);        // dQ^T = K^T dS^T: both MN-major
-      const uint32_t dK_k = sdesc_lo(sK, 16), dV_k = sdesc_lo(sV, 16), dQ_k = sdesc_lo(sQ, 16);
-      const uint32_t dDO_k = sdesc_lo(sDO, 16), dDS_k = sdesc_lo(sDS, 16), dDS_mn = sdesc_lo(sDS, 16384);
-      // K-major steps of 16 columns cross a 64-column box every 4 steps (K / V boxes
-      // hold 128 rows, Q / dO boxes QR rows); MN-major steps advance 16 rows
-      auto kstep_kv = [](int kk) { return uint32_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
-      auto kstep_q = [](int kk) { return uint32_t(((kk >> 2) * Cfg::kQBox + (kk & 3) * 32) >> 4); };
-      auto mnstep = [](int kk) { return uint32_t((kk * 2048) >> 4); };
-      uint32_t u = 0, ua = 0, sc = 0;
-      bool ok = true;
-      for (uint32_t uk = 0; ok; ++uk) {
-        const int w = unit_take(bar(C_UFULL), bar(C_UEMPTY), unit_ring, uk, abort_flag, true);
-        if (w == -2) ok = false;
-        if (w < 0) break;
-        const int32_t* W = work + w * kBwdWords;
-        const int nsteps = W[W_NQ];
-        if (nsteps == 0) continue;
-        if (!(ok = mbar_wait(bar(C_KVFULL), u & 1, abort_flag))) break;
-        auto issue_s = [&](uint32_t step) {  // S^T = K Q^T (one Q stage)
-          if (!(ok = mbar_wait(bar(C_QFULL0), step & 1, abort_flag))) return;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss_lo(tmem, dK_k + kstep_kv(kk), dQ_k + kstep_q(kk), idS, kk > 0);
-          tc_commit(bar(C_SFULL));
-        };
-        for (int e = 0; e < 2 && ok; ++e) {
-          const uint32_t dKe_mn = sdesc_lo(sK + e * 2 * 16384, 16384);             // K^T rows of this half
-          const uint32_t dDOe_mn = sdesc_lo(sDO + e * 2 * Cfg::kQBox, Cfg::kQBox);  // dO columns of this half
-          const uint32_t dQe_mn = sdesc_lo(sQ + e * 2 * Cfg::kQBox, Cfg::kQBox);    // Q columns of this half
-          issue_s(sc);
-          for (int s = 0; s < nsteps && ok; ++s, ++sc) {
-            if (!(ok = mbar_wait(bar(C_DOFULL), sc & 1, abort_flag))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss_lo(tmem + Cfg::kColDP, dV_k + kstep_kv(kk), dDO_k + kstep_q(kk), idS, kk > 0);
-            tc_commit(bar(C_DPFULL));
-            if (!(ok = mbar_wait(bar(C_PREADY), sc & 1, abort_flag))) break;
-            if (s == 0 && !(ok = mbar_wait(bar(C_DVFREE), (ua & 1) ^ 1, abort_flag))) break;
-            tc_fence_after();
-            // P^T in TMEM: the query half h of the step packed into columns [QR/2 h, QR/2 h + QR/4)
-#pragma unroll
-            for (int kk = 0; kk < QR / 16; ++kk)
-              mma_ts_lo(tmem + Cfg::kColDV, tmem + (kk >> 1) * (QR / 2) + (kk & 1) * 8, dDOe_mn + mnstep(kk), idAcc,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C_DOEMPTY));
-            if (!(ok = mbar_wait(bar(C_DSREADY), sc & 1, abort_flag))) break;
-            if (s == 0 && !(ok = mbar_wait(bar(C_DKFREE), (ua & 1) ^ 1, abort_flag))) break;
-            tc_fence_after();
-            // dK first: it is the last reader of the Q stage, whose next tile then
-            // loads while dQ^T runs
-#pragma unroll
-            for (int kk = 0; kk < QR / 16; ++kk)
-              mma_ss_lo(tmem + Cfg::kColDK, dDS_k + 2 * kk, dQe_mn + mnstep(kk), idAcc, (s > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C_QEMPTY0));
-            if (s == nsteps - 1) tc_commit(bar(C_ACCDONE));
-            if (!(ok = mbar_wait(bar(C_DQEMPTY), (sc & 1) ^ 1, abort_flag))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss_lo(tmem + Cfg::kColDQ, dKe_mn + mnstep(kk), dDS_mn + mnstep(kk), idDQ, kk > 0);
-            tc_commit(bar(C_DQFULL));
-            tc_commit(bar(C_DSFREE));
-            if (s == nsteps - 1) {
-              if (e == 1) tc_commit(bar(C_KVEMPTY));
-            } else {
-              issue_s(sc + 1);
-            }
-          }
-          ++ua;
-        }
-        ++u;
-      }
-      if (!ok) {
-        tc_commit(bar(C_DRAIN));
-        mbar_wait_drain(bar(C_DRAIN), 0);
-      }
     }
    }
   } else if (warp < 12) {
@@ -452,22 +307,20 @@ __global__ void __launch_bounds__(512, 1)
       if (W[W_NQ] == 0) continue;
       const int32_t* I0 = items + W[W_ITEM_LO] * kItemWords;
       const int j = I0[I_KVBASE] + W[W_KTILE] * 128 + jl;  // global key row
-      const StepRange<Cfg::kQRows> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
-      constexpr int QR = Cfg::kQRows, QS = Cfg::kQStages, NCH = QR / 64;  // 32-query chunks per warp
-      for (int pass = 0; pass < Cfg::kPasses && ok; ++pass)
+      const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
       for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
         int t0, t1, r0;
         if (!R.tiles(it, t0, t1, r0)) continue;
         const uint32_t bseq = uint32_t(items[it * kItemWords + I_B]);
         for (int t = t0; t <= t1 && ok; ++t)
           for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
-            const int qs = sc % QS;
+            const int qs = sc & 1;
             const uint32_t hq = uint32_t(W[W_G] * a.G + hh);  // query head
-            const int i0 = r0 + t * QR;  // global row of query column 0
+            const int i0 = r0 + t * 128;  // global row of query column 0
             const float* st_lse = reinterpret_cast<const float*>(smem + Cfg::kOffStat + qs * Cfg::kStatBytes);
-            const float* st_d = st_lse + QR;
-            const int32_t* st_ds = reinterpret_cast<const int32_t*>(st_lse + 2 * QR);
-            if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc / QS) & 1, abort_flag))) break;
+            const float* st_d = st_lse + 128;
+            const int32_t* st_ds = reinterpret_cast<const int32_t*>(st_lse + 256);
+            if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
             if (threadIdx.x == 128) BD_TRACE_EVENT(10, int(sc));  // compute: waits S
             if (!(ok = mbar_wait(bar(C_SFULL), sc & 1, abort_flag))) break;
             if (threadIdx.x == 128) BD_TRACE_EVENT(11, int(sc));  // compute: S ready
@@ -475,19 +328,18 @@ __global__ void __launch_bounds__(512, 1)
             // Rows' document starts are non-decreasing and invalid rows carry
             // INT_MAX, so key j sees every query of the tile iff it lies at or
             // before the tile's first row and at or after the last row's doc start.
-            const bool full = (j <= i0) && (j >= st_ds[QR - 1]);
+            const bool full = (j <= i0) && (j >= st_ds[127]);
             // P^T is kept as the bf16 pairs written to TMEM (the dV MMA reads the same
             // rounded values); dS below unpacks them
-            uint32_t pk[NCH][16];
-            uint32_t keep[NCH];  // dropout: bit e of chunk ch keeps query i0 + ib + e
+            uint32_t pk[2][16];
+            uint32_t keep[2] = {0u, 0u};  // dropout: bit e of chunk ch keeps query i0 + ib + e
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
               uint32_t r[32];
-              tmem_ld32(tmem + lane_base + half * (QR / 2) + ch * 32, r);
+              tmem_ld32(tmem + lane_base + half * 64 + ch * 32, r);
               tmem_ld_wait();
               reg_fence(r);
-              const int ib = half * (QR / 2) + ch * 32;
-              keep[ch] = 0u;
+              const int ib = half * 64 + ch * 32;
               float p[32];
 #pragma unroll
               for (int e4 = 0; e4 < 8; ++e4) {
@@ -551,9 +403,9 @@ __global__ void __launch_bounds__(512, 1)
                 for (int e = 0; e < 16; ++e)
                   pd[e] = pack_bf16(((kb >> (2 * e)) & 1) ? p[2 * e] * a.drop_scale : 0.f,
                                     ((kb >> (2 * e + 1)) & 1) ? p[2 * e + 1] * a.drop_scale : 0.f);
-                tmem_st16(tmem + lane_base + half * (QR / 2) + ch * 16, pd);
+                tmem_st16(tmem + lane_base + half * 64 + ch * 16, pd);
               } else {
-                tmem_st16(tmem + lane_base + half * (QR / 2) + ch * 16, pk[ch]);
+                tmem_st16(tmem + lane_base + half * 64 + ch * 16, pk[ch]);
               }
             }
             tmem_st_wait();
@@ -564,22 +416,17 @@ __global__ void __launch_bounds__(512, 1)
             if (threadIdx.x == 128) BD_TRACE_EVENT(13, int(sc));  // compute: dP ready
             tc_fence_after();
             // dS^T of the previous step must have been consumed by its dQ and dK MMAs
-            // (the later of the two commits the stage's QEMPTY, or DSFREE for dQ^T)
-            if (sc > 0 && !(ok = Cfg::kDqT ? mbar_wait(bar(C_DSFREE), (sc - 1) & 1, abort_flag)
-                                           : mbar_wait(bar(C_QEMPTY0 + ((sc - 1) % QS)), ((sc - 1) / QS) & 1,
-                                                       abort_flag)))
+            // (dK is the later one; its commit also releases that step's Q stage)
+            if (sc > 0 && !(ok = mbar_wait(bar(C_QEMPTY0 + ((sc - 1) & 1)), ((sc - 1) >> 1) & 1, abort_flag)))
               break;
+            const uint32_t row_addr = sDS + half * 16384 + jl * 128;
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
               uint32_t r[32];
-              tmem_ld32(tmem + lane_base + Cfg::kColDP + half * (QR / 2) + ch * 32, r);
+              tmem_ld32(tmem + lane_base + Cfg::kColDP + half * 64 + ch * 32, r);
               tmem_ld_wait();
               reg_fence(r);
-              const int ib = half * (QR / 2) + ch * 32;
-              // dS^T rows are 64-query blocks of 128 bytes (128-byte swizzle); this
-              // chunk's 32 queries are 16-byte pieces cb .. cb + 3 of block ib / 64
-              const uint32_t row_addr = sDS + (ib >> 6) * 16384 + jl * 128;
-              const int cb = (ib & 63) >> 3;
+              const int ib = half * 64 + ch * 32;
               uint32_t dsk[16];
 #pragma unroll
               for (int e4 = 0; e4 < 8; ++e4) {
@@ -602,7 +449,7 @@ __global__ void __launch_bounds__(512, 1)
               }
 #pragma unroll
               for (int c4 = 0; c4 < 4; ++c4) {
-                const int chunk = cb + c4;  // 16-byte chunk of the 128-byte row
+                const int chunk = ch * 4 + c4;  // 16-byte chunk of the 128-byte row
                 st_shared_v4(row_addr + ((chunk ^ (jl & 7)) << 4), dsk[4 * c4], dsk[4 * c4 + 1], dsk[4 * c4 + 2],
                              dsk[4 * c4 + 3]);
               }
@@ -617,9 +464,9 @@ __global__ void __launch_bounds__(512, 1)
     regs_set<Cfg::kRegsDq, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ dQ out, dK/dV epilogue
     const int quarter = warp & 3;
-    const int rl = quarter * 32 + lane;  // TMEM lane: query row of dQ (column of dQ^T), key row of dK / dV
+    const int rl = quarter * 32 + lane;  // query row (dQ) or key row (dK/dV) == TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    uint32_t ua = 0, sc = 0;  // accumulation passes, steps
+    uint32_t u = 0, sc = 0;
     bool ok = true;
     for (uint32_t uk = 0; ok; ++uk) {
       const int w = unit_take(bar(C_UFULL), bar(C_UEMPTY), unit_ring, uk, abort_flag, false);
@@ -641,134 +488,97 @@ __global__ void __launch_bounds__(512, 1)
         }
         continue;
       }
-      const StepRange<Cfg::kQRows> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
-      for (int pass = 0; pass < Cfg::kPasses && ok; ++pass) {
-        for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
-          int t0, t1, r0;
-          if (!R.tiles(it, t0, t1, r0)) continue;
-          const int32_t* I = items + it * kItemWords;
-          const int b = I[I_B], c = I[I_C];
-          for (int t = t0; t <= t1 && ok; ++t)
-            for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
-              const int h = g * a.G + hh;
-              // the warpgroup meets at named barriers below: leave together or not at all
-              if (rl == 0) BD_TRACE_EVENT(20, int(sc));  // dQ: waits dQ
-              ok = bar_red_and(1, 128, mbar_wait(bar(C_DQFULL), sc & 1, abort_flag));
-              if (rl == 0) BD_TRACE_EVENT(21, int(sc));  // dQ: dQ ready
-              if (!ok) break;
-              tc_fence_after();
-              if constexpr (Cfg::kDqT) {
-                // dQ^T of this pass's columns: lane rl holds column 128 pass + rl of the
-                // step's QR query rows. Each warp turns its 32 columns into row-major
-                // 16-row x 32-column boxes (128-byte rows, 128-byte swizzle: 16-byte
-                // chunk c of row q sits at c ^ (q & 7)) in two buffers of its own and
-                // sends each with a TMA reduce-add (rows past L are clipped by the map)
-                constexpr int QR = Cfg::kQRows;
-                uint32_t r[QR / 32][32];
+      const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
+      for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+        int t0, t1, r0;
+        if (!R.tiles(it, t0, t1, r0)) continue;
+        const int32_t* I = items + it * kItemWords;
+        const int b = I[I_B], c = I[I_C], svalid = I[I_SVALID];
+        for (int t = t0; t <= t1 && ok; ++t)
+          for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+            const int h = g * a.G + hh;
+            const int lrow = t * 128 + rl;
+            // the warpgroup meets at named barriers below: leave together or not at all
+            if (rl == 0) BD_TRACE_EVENT(20, int(sc));  // dQ: waits dQ
+            ok = bar_red_and(1, 128, mbar_wait(bar(C_DQFULL), sc & 1, abort_flag));
+            if (rl == 0) BD_TRACE_EVENT(21, int(sc));  // dQ: dQ ready
+            if (!ok) break;
+            tc_fence_after();
+            // dQ tile (128 query rows x D fp32) goes to global memory as TMA
+            // reduce-adds (rows past L are clipped by the map); the whole dQ row
+            // leaves TMEM first, so the next dP^T can start at once
+            uint32_t r[D / 32][32];
 #pragma unroll
-                for (int q = 0; q < QR / 32; ++q) tmem_ld32(tmem + lane_base + Cfg::kColDQ + q * 32, r[q]);
-                tmem_ld_wait();
+            for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + Cfg::kColDP + q * 32, r[q]);
+            tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < QR / 32; ++q) reg_fence(r[q]);
-                tc_fence_before();
-                mbar_arrive(bar(C_DQEMPTY));
+            for (int q = 0; q < D / 32; ++q) reg_fence(r[q]);
+            tc_fence_before();
+            mbar_arrive(bar(C_DQEMPTY));
+            if (rl == 0) BD_TRACE_EVENT(22, int(sc));  // dQ: TMEM released
+            // D/16 rounds of 128 rows x 16 columns through two 8 KB staging buffers
+            // (64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)), so
+            // that filling one buffer overlaps the TMA reading the other
 #pragma unroll
-                for (int rr = 0; rr < QR / 16; ++rr) {
-                  const uint32_t buf = sStage + (quarter * 2 + (rr & 1)) * 2048;
-                  if (lane == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
-                  __syncwarp();
+            for (int q = 0; q < D / 16; ++q) {
+              const uint32_t buf = sStage + (q & 1) * 8192;
+              if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
+              named_bar_sync(1, 128);
+              const uint32_t* v = r[q >> 1] + (q & 1) * 16;
 #pragma unroll
-                  for (int q = 0; q < 16; ++q) {
-                    const int row = rr * 16 + q;
-                    st_shared_f32(buf + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4,
-                                  __uint_as_float(r[row >> 5][row & 31]) * a.scale);
-                  }
-                  fence_proxy_async_smem();
-                  __syncwarp();
-                  if (lane == 0) {
-                    tma_reduce_add_5d(&tm_dq, buf, pass * Cfg::kDH + quarter * 32, h, t * QR + rr * 16, c, b);
-                    bulk_commit();
-                  }
-                }
-              } else {
-                // dQ tile (128 query rows x D fp32) goes to global memory as TMA
-                // reduce-adds (rows past L are clipped by the map); the whole dQ row
-                // leaves TMEM first, so the next dP^T can start at once
-                uint32_t r[D / 32][32];
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + Cfg::kColDQ + q * 32, r[q]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) reg_fence(r[q]);
-                tc_fence_before();
-                mbar_arrive(bar(C_DQEMPTY));
-                if (rl == 0) BD_TRACE_EVENT(22, int(sc));  // dQ: TMEM released
-                // D/16 rounds of 128 rows x 16 columns through two 8 KB staging buffers
-                // (64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)), so
-                // that filling one buffer overlaps the TMA reading the other
-#pragma unroll
-                for (int q = 0; q < D / 16; ++q) {
-                  const uint32_t buf = sStage + (q & 1) * 8192;
-                  if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
-                  named_bar_sync(1, 128);
-                  const uint32_t* v = r[q >> 1] + (q & 1) * 16;
-#pragma unroll
-                  for (int c4 = 0; c4 < 4; ++c4)
-                    st_shared_v4(buf + rl * 64 + ((c4 ^ ((rl >> 1) & 3)) << 4),
-                                 __float_as_uint(__uint_as_float(v[4 * c4]) * a.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * a.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * a.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * c4 + 3]) * a.scale));
-                  fence_proxy_async_smem();
-                  named_bar_sync(1, 128);
-                  if (rl == 0) {
-                    tma_reduce_add_5d(&tm_dq, buf, q * 16, h, t * 128, c, b);
-                    bulk_commit();
-                  }
-                }
+              for (int c4 = 0; c4 < 4; ++c4)
+                st_shared_v4(buf + rl * 64 + ((c4 ^ ((rl >> 1) & 3)) << 4),
+                             __float_as_uint(__uint_as_float(v[4 * c4]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[4 * c4 + 3]) * a.scale));
+              fence_proxy_async_smem();
+              named_bar_sync(1, 128);
+              if (rl == 0) {
+                tma_reduce_add_5d(&tm_dq, buf, q * 16, h, t * 128, c, b);
+                bulk_commit();
               }
             }
-        }
-        if (!ok) break;
-        if (!(ok = mbar_wait(bar(C_ACCDONE), ua & 1, abort_flag))) break;
-        tc_fence_after();
-        // dV, then dK (x scale), columns [kDH pass, kDH pass + kDH): each block leaves
-        // TMEM whole before it is stored, so that the next pass's or unit's first
-        // dV / dK MMA can start while the rows go out
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          uint32_t v[Cfg::kDH / 32][32];
-#pragma unroll
-          for (int q = 0; q < Cfg::kDH / 32; ++q)
-            tmem_ld32(tmem + lane_base + (x ? Cfg::kColDK : Cfg::kColDV) + q * 32, v[q]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < Cfg::kDH / 32; ++q) reg_fence(v[q]);
-          tc_fence_before();
-          mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
-          if (krow_ok) {
-            float* row = (x ? dkrow : dvrow) + pass * Cfg::kDH;
-            const float mul = x ? a.scale : 1.f;
-#pragma unroll
-            for (int q = 0; q < Cfg::kDH / 32; ++q)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
-                                       __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
-                float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
-                if (a.accumulate) {
-                  const float4 old = *p;
-                  o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                }
-                *p = o;
-              }
+            (void)lrow;
+            (void)svalid;
           }
-        }
-        ++ua;
       }
       if (!ok) break;
+      if (!(ok = mbar_wait(bar(C_ACCDONE), u & 1, abort_flag))) break;
+      tc_fence_after();
+      // dV, then dK (x scale): each block leaves TMEM whole before it is stored, so
+      // that the next unit's first dV / dK MMA can start while the rows go out
+#pragma unroll 1
+      for (int x = 0; x < 2; ++x) {
+        uint32_t v[D / 32][32];
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + (x ? Cfg::kColDK : Cfg::kColDV) + q * 32, v[q]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) reg_fence(v[q]);
+        tc_fence_before();
+        mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
+        if (krow_ok) {
+          float* row = x ? dkrow : dvrow;
+          const float mul = x ? a.scale : 1.f;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
+                                     __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
+              float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
+              if (a.accumulate) {
+                const float4 old = *p;
+                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              }
+              *p = o;
+            }
+        }
+      }
+      ++u;
     }
-    if (Cfg::kDqT ? lane == 0 : rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
+    if (rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
   }
 
   tc_fence_before();
@@ -926,11 +736,11 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
   CUtensorMap mq, mk, mv, mdo, mdq;
   // dQ reduce boxes: 128 rows x 16 columns (64-byte swizzle), or at head dim 256
-  // (transposed dQ) 16 rows x 32 columns (128-byte swizzle)
+  // (transposed dQ) 16 rows x 32 columns (128-byte swizzle); Q / dO boxes are one
+  // backward query step high
   if ((st = c.D == 256 ? make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 16)
                        : make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq")))
     return st;
-  // Q / dO boxes are one backward query step high
   if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q", bwd_query_step(c.D)))) return st;
   if ((st = make_tmap_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout", bwd_query_step(c.D)))) return st;
   if ((st = make_tmap_bf16(&mk, k, c.B, c.Ck, c.Hkv, c.D, "k"))) return st;
@@ -964,14 +774,14 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   a.drop_k1 = uint32_t(pv.hdr(H_DROP_SEED_HI));
   const int32_t dbits = pv.hdr(H_DROP_SCALE_BITS);
   memcpy(&a.drop_scale, &dbits, 4);
-  if (a.drop_thresh != 0)
-    st = c.D == 256   ? launch_bwd<256, true>(mq, mk, mv, mdo, mdq, a, grid, s)
-         : c.D == 128 ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, a, grid, s)
-                      : launch_bwd<64, true>(mq, mk, mv, mdo, mdq, a, grid, s);
+  if (c.D == 256)
+    st = launch_bwd256(mq, mk, mv, mdo, mdq, a, a.drop_thresh != 0, grid, s);
+  else if (a.drop_thresh != 0)
+    st = c.D == 128 ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, a, grid, s)
+                    : launch_bwd<64, true>(mq, mk, mv, mdo, mdq, a, grid, s);
   else
-    st = c.D == 256   ? launch_bwd<256, false>(mq, mk, mv, mdo, mdq, a, grid, s)
-         : c.D == 128 ? launch_bwd<128, false>(mq, mk, mv, mdo, mdq, a, grid, s)
-                      : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, a, grid, s);
+    st = c.D == 128 ? launch_bwd<128, false>(mq, mk, mv, mdo, mdq, a, grid, s)
+                    : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, a, grid, s);
   if (st) return st;
   return ok();
 }
