@@ -136,3 +136,30 @@ def test_d256_accumulate_into_shared_kv():
     _, gk, gv, _, _ = oracle.attention_bwd(q[0], k[0], v[0], do[0], wl.cu[0])
     assert gu.max_rel((dk - base)[0, 0].cpu(), gk) <= gu.GRAD_REL
     assert gu.max_rel((dv - 2 * base)[0, 0].cpu(), gv) <= gu.GRAD_REL
+
+
+@pytest.mark.parametrize("i", [3, 4])
+def test_d256_sampled_full_size(i):
+    """The 16k lognormal and 49k single-document workloads at head dim 256, in the
+    launch configuration the benchmark times with --head-dim 256 (needed-only
+    windows for the 16k layout, owner sums): O, LSE and dQ on sampled rows, dK and
+    dV on sampled key columns, against the row / column oracles."""
+    import numpy as np
+    from test_gpu_bwd import _sample_cols, run_bwd
+    wl = dataclasses.replace(workloads.config(i), d=256)
+    mode = bd.BD_KV_WINDOW if wl.kv_mode == "window" else bd.BD_KV_GATHER
+    q, k, v, do = workloads.tensors(wl)
+    plan, out, lse, _ = gu.run_fwd(wl, q, k, v, mode)
+    out = out.cpu().view(wl.B, wl.S, wl.H, wl.d)
+    lse = lse.cpu().permute(0, 2, 1, 3).reshape(wl.B, wl.H, wl.S)
+    dq, dk, dv = run_bwd(wl, q, k, v, do, mode)
+    b, cu = 0, wl.cu[0]
+    rows = gu.sample_rows(wl, b, n_rand=8 if i == 4 else 16)
+    o_r, l_r = oracle.attention_fwd(q[b], k[b], v[b], cu, rows=rows)
+    gu.o_check(out[b, rows].float(), o_r)
+    gu.lse_check(lse[b][:, rows], l_r)
+    assert gu.max_rel(dq[b, rows], oracle.attention_bwd_rows(q[b], k[b], v[b], do[b], cu, rows)) <= gu.GRAD_REL
+    cols = _sample_cols(wl, b, np.random.default_rng(i), n_tail=8, n_rand=8)
+    gk, gv = oracle.attention_bwd_cols(q[b], k[b], v[b], do[b], cu, cols)
+    assert gu.max_rel(dk[b, cols], gk) <= gu.GRAD_REL
+    assert gu.max_rel(dv[b, cols], gv) <= gu.GRAD_REL
