@@ -14,7 +14,9 @@
 //   pass 0  S^T = K Q^T, P^T, dV += P^T dO            (dV in TMEM columns 256..511)
 //   pass 1  S^T, dP^T = V dO^T, dS^T, dK += dS^T Q,   (dK in the same columns)
 //           dQ^T = K^T dS^T (two 128-row halves of d)
-// S^T is recomputed in pass 1; every other product is formed once.
+// S^T is recomputed in pass 1; every other product is formed once. Pass 1 walks
+// the steps in reverse order, so that it starts on the Q / dO tiles pass 0 read
+// last, which are the ones still in L2.
 // Roles (16 warps, one persistent CTA per SM claiming units dynamically):
 //   warp 0       TMA producer: K/V once per unit; per step the Q and dO tiles
 //                (64 rows x 256) and, into a two-stage ring of their own, the
@@ -141,13 +143,15 @@ __global__ void __launch_bounds__(512, 1)
           ++u;
           const StepRange<QR> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
           for (int pass = 0; pass < 2 && ok; ++pass)
-            for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+            for (int ii = 0; ii < R.it_hi - R.it_lo && ok; ++ii) {
+              const int it = pass ? R.it_hi - 1 - ii : R.it_lo + ii;
               int t0, t1, r0;
               if (!R.tiles(it, t0, t1, r0)) continue;
               const int32_t* I = items + it * kItemWords;
               const int b = I[I_B], c = I[I_C];
-              for (int t = t0; t <= t1 && ok; ++t)
-                for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+              for (int tt = 0; tt <= t1 - t0 && ok; ++tt)
+                for (int h2 = 0; h2 < a.G && ok; ++h2, ++sc) {
+                  const int t = pass ? t1 - tt : t0 + tt, hh = pass ? a.G - 1 - h2 : h2;
                   const int h = g * a.G + hh;
                   // row statistics into their own two-stage ring
                   const int ss = sc & 1;
@@ -293,12 +297,14 @@ __global__ void __launch_bounds__(512, 1)
       const int j = I0[I_KVBASE] + W[W_KTILE] * 128 + jl;  // global key row
       const StepRange<QR> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
       for (int pass = 0; pass < 2 && ok; ++pass)
-        for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+        for (int ii = 0; ii < R.it_hi - R.it_lo && ok; ++ii) {
+          const int it = pass ? R.it_hi - 1 - ii : R.it_lo + ii;
           int t0, t1, r0;
           if (!R.tiles(it, t0, t1, r0)) continue;
           const uint32_t bseq = uint32_t(items[it * kItemWords + I_B]);
-          for (int t = t0; t <= t1 && ok; ++t)
-            for (int hh = 0; hh < a.G && ok; ++hh, ++sc) {
+          for (int tt = 0; tt <= t1 - t0 && ok; ++tt)
+            for (int h2 = 0; h2 < a.G && ok; ++h2, ++sc) {
+              const int t = pass ? t1 - tt : t0 + tt, hh = pass ? a.G - 1 - h2 : h2;
               const int ss = sc & 1;
               const uint32_t hq = uint32_t(W[W_G] * a.G + hh);  // query head
               const int i0 = r0 + t * QR;                        // global row of query column 0
@@ -467,13 +473,15 @@ __global__ void __launch_bounds__(512, 1)
       const StepRange<QR> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
-          for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
+          for (int ii = 0; ii < R.it_hi - R.it_lo && ok; ++ii) {
+            const int it = R.it_hi - 1 - ii;
             int t0, t1, r0;
             if (!R.tiles(it, t0, t1, r0)) continue;
             const int32_t* I = items + it * kItemWords;
             const int b = I[I_B], c = I[I_C];
-            for (int t = t0; t <= t1 && ok; ++t)
-              for (int hh = 0; hh < a.G && ok; ++hh, ++s1) {
+            for (int tt = 0; tt <= t1 - t0 && ok; ++tt)
+              for (int h2 = 0; h2 < a.G && ok; ++h2, ++s1) {
+                const int t = t1 - tt, hh = a.G - 1 - h2;
                 const int h = g * a.G + hh;
                 // lanes of a warp leave together (they meet at __syncwarp below)
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(E_DQFULL), s1 & 1, abort_flag));

@@ -154,8 +154,7 @@ BD_API int32_t bd_exchange_plan(const int32_t* cu_seqlens, int32_t ndocs, int32_
 typedef struct {
   int32_t B, S, cp, nchunks;
   const int32_t* ranks;       /* host int32[nchunks] or NULL                      */
-  int32_t H, Hkv, d;          /* d in {64, 128, 256} (256: forward only);
-                                 H % Hkv == 0                                     */
+  int32_t H, Hkv, d;          /* d in {64, 128, 256}; H % Hkv == 0               */
   int32_t kv_mode;            /* bd_kv_mode                                       */
   const int32_t* cu_seqlens;  /* host: all sequences' cu arrays back to back      */
   const int32_t* cu_offsets;  /* host int32[B+1]: sequence b's array is
