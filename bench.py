@@ -341,15 +341,12 @@ def run_ours(args):
         ev[2].record(stream)
         bd.bd_attn_bwd_main(plan, qd, kd, vd, dod, dq, dk, dv, wsp, stream=stream)
         ev[3].record(stream)
-        if mode == bd.BD_KV_WINDOW:
-            bd.bd_owner_sum(plan, dk, dv, dk_own, dv_own, stream=stream)
+        if mode == bd.BD_KV_WINDOW:  # stores every owner row: nothing to clear between steps
+            bd.bd_owner_sum(plan, dk, dv, dk_own, dv_own, stream=stream, accumulate=False)
         ev[4].record(stream)
 
     def prep():
         flush.zero_()
-        if mode == bd.BD_KV_WINDOW:
-            dk_own.zero_()
-            dv_own.zero_()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     warm = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -431,14 +428,11 @@ def run_ours(args):
                 in_ready[i].record(s_in)
             stream.wait_event(in_ready[i])
             stream.wait_event(out_done[i])               # step t-2's results have left this set
-            if mode == bd.BD_KV_WINDOW:
-                D_["dk"].zero_()
-                D_["dv"].zero_()
             bd.bd_attn_fwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
             bd.bd_attn_bwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
                            D_["dvw"], D_["ws"], stream=stream)
             if mode == bd.BD_KV_WINDOW:
-                bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream)
+                bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream, accumulate=False)
             comp_done[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[i])

@@ -247,10 +247,13 @@ def bd_attn_bwd_main(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, accumulat
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None):
-    """Add needed-only-window dK/dV partials into owner rows (see include/bd_attn.h)."""
+def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None, accumulate=True):
+    """Sum needed-only-window dK/dV partials at their owner rows, added into dk/dv
+    (accumulate=True) or stored there (accumulate=False: every owner row is
+    written); see include/bd_attn.h."""
     ts = [_tensor(x, n) for x, n in ((dk_win, "dk_win"), (dv_win, "dv_win"), (dk, "dk"), (dv, "dv"))]
-    check(load().bd_owner_sum(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], _stream(stream)))
+    check(load().bd_owner_sum_ex(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], int(bool(accumulate)),
+                                 _stream(stream)))
 
 
 def bd_check_status(plan: Plan, reset: bool = True, stream=None):

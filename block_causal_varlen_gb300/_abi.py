@@ -102,6 +102,8 @@ EXPORTS = {
     "bd_attn_bwd_noalloc_capacity": (C.c_size_t, []),
     "bd_owner_sum": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                  C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_void_p]),
+    "bd_owner_sum_ex": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                    C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_int32, C.c_void_p]),
     "bd_check_status": (C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p]),
     "bd_selftest_bounded_wait": (C.c_int32, [C.c_void_p, C.c_uint32, C.c_void_p]),
     "bd_last_error": (C.c_char_p, []),

@@ -108,7 +108,9 @@ int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
   return e == cudaSuccess ? BD_OK : cuda_fail(e, "bd_bwd_pre_kernel launch");
 }
 
-// One thread per (b, global row, head, 4 columns): sums the chunks' windows in order.
+// One thread per (b, global row, head, 4 columns): sums the chunks' windows in order
+// and adds the sum into the owner row, or stores it there (every owner row is
+// written, rows no window covers with zeros).
 __global__ void __launch_bounds__(256) bd_owner_sum_kernel(OwnerSumArgs a) {
   const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int q4 = a.d / 4;
@@ -133,11 +135,13 @@ __global__ void __launch_bounds__(256) bd_owner_sum_kernel(OwnerSumArgs a) {
   }
   float4* pk = reinterpret_cast<float4*>(a.dk + b * a.k_sb + int64_t(row) * a.k_sr + int64_t(h) * a.k_sh + col);
   float4* pv = reinterpret_cast<float4*>(a.dv + b * a.v_sb + int64_t(row) * a.v_sr + int64_t(h) * a.v_sh + col);
-  float4 ok = *pk, ov = *pv;
-  ok.x += sk.x; ok.y += sk.y; ok.z += sk.z; ok.w += sk.w;
-  ov.x += sv.x; ov.y += sv.y; ov.z += sv.z; ov.w += sv.w;
-  *pk = ok;
-  *pv = ov;
+  if (a.accumulate) {
+    const float4 ok = *pk, ov = *pv;
+    sk.x += ok.x; sk.y += ok.y; sk.z += ok.z; sk.w += ok.w;
+    sv.x += ov.x; sv.y += ov.y; sv.z += ov.z; sv.w += ov.w;
+  }
+  *pk = sk;
+  *pv = sv;
 }
 
 // Waits, with the kernels' bounded wait, on an mbarrier that nothing arrives at,
@@ -172,8 +176,9 @@ extern "C" int32_t bd_selftest_bounded_wait(const void* plan_dev, uint32_t limit
   return ok();
 }
 
-extern "C" int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
-                                const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream) {
+extern "C" int32_t bd_owner_sum_ex(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
+                                   const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, int32_t accumulate,
+                                   void* stream) {
   PlanView pv;
   int32_t st = view_plan(plan_host, &pv);
   if (st) return st;
@@ -197,12 +202,17 @@ extern "C" int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, con
   a.wv_sb = dv_win->stride_b; a.wv_sc = dv_win->stride_c; a.wv_sr = dv_win->stride_row; a.wv_sh = dv_win->stride_head;
   a.k_sb = dk->stride_b; a.k_sr = dk->stride_row; a.k_sh = dk->stride_head;
   a.v_sb = dv->stride_b; a.v_sr = dv->stride_row; a.v_sh = dv->stride_head;
-  a.B = B; a.C = C; a.S = S; a.Hkv = Hkv; a.d = D;
+  a.B = B; a.C = C; a.S = S; a.Hkv = Hkv; a.d = D; a.accumulate = accumulate ? 1 : 0;
   const int64_t total = int64_t(B) * S * Hkv * (D / 4);
   bd_owner_sum_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_owner_sum_kernel launch");
   return ok();
+}
+
+extern "C" int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
+                                const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream) {
+  return bd_owner_sum_ex(plan_host, plan_dev, dk_win, dv_win, dk, dv, 1, stream);
 }
 
 extern "C" int32_t bd_check_status(const void* plan_dev, int32_t reset, void* stream) {

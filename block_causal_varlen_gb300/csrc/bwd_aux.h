@@ -37,6 +37,7 @@ struct OwnerSumArgs {
   int64_t wk_sb, wk_sc, wk_sr, wk_sh, wv_sb, wv_sc, wv_sr, wv_sh;
   int64_t k_sb, k_sr, k_sh, v_sb, v_sr, v_sh;
   int32_t B, C, S, Hkv, d;
+  int32_t accumulate;  // 1: add the sum into dk / dv; 0: overwrite them with it
 };
 
 int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s);

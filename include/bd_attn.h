@@ -278,6 +278,14 @@ BD_API int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, con
 BD_API int32_t bd_owner_sum(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
                      const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, void* stream);
 
+/* bd_owner_sum_ex -- bd_owner_sum with accumulate = 0 storing the sum instead
+ * of adding it: every owner row of dk/dv is written (rows no window covers,
+ * i.e. padding, get zeros), so they need no clearing and are not read.
+ * accumulate = 1 is bd_owner_sum. */
+BD_API int32_t bd_owner_sum_ex(const void* plan_host, const void* plan_dev, const bd_tensor* dk_win,
+                        const bd_tensor* dv_win, bd_tensor* dk, bd_tensor* dv, int32_t accumulate,
+                        void* stream);
+
 /* bd_attn_bwd_noalloc -- bd_attn_bwd for callers that cannot allocate device
  * memory (no allocator is available to them, or a memory cap forbids one
  * more allocation). The paper has no counterpart: it is an addition of this

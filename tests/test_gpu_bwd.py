@@ -254,3 +254,29 @@ def test_pre_without_clearing_after_caller_zeroes_dq():
     (dq1, dk1, dv1), (dq2, dk2, dv2) = res
     assert torch.isfinite(dq2).all() and gu.max_rel(dq2, dq1) < 1e-5
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+
+
+def test_owner_sum_store_writes_every_owner_row():
+    """bd_owner_sum_ex with accumulate = 0 stores the window sums into owner
+    buffers that start as NaN: every row is written (padding rows with zeros) and
+    the result equals adding into zeroed buffers, bit for bit."""
+    wl = workloads.config(3)
+    q, k, v, do = workloads.tensors(wl)
+    plan, out, lse, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, bd.BD_KV_WINDOW)
+    dod = gu.as_chunks(do.cuda(), wl.cp)
+    dq = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    dk = torch.zeros(kd.shape, dtype=torch.float32, device="cuda")
+    dv = torch.zeros_like(dk)
+    ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
+    bd.bd_attn_bwd(plan, qd, kd, vd, out, dod, lse, dq, dk, dv, ws)
+    shape = (wl.B, 1, wl.S, wl.Hkv, wl.d)
+    add_k = torch.zeros(shape, dtype=torch.float32, device="cuda")
+    add_v = torch.zeros_like(add_k)
+    bd.bd_owner_sum(plan, dk, dv, add_k, add_v)
+    st_k = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    st_v = torch.full_like(st_k, float("nan"))
+    bd.bd_owner_sum(plan, dk, dv, st_k, st_v, accumulate=False)
+    torch.cuda.synchronize()
+    assert torch.equal(st_k, add_k) and torch.equal(st_v, add_v)
+    pad = wl.cu[0][-1]
+    assert not st_k[0, 0, pad:].any() and not st_v[0, 0, pad:].any()

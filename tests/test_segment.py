@@ -204,3 +204,62 @@ def test_plan_row_doc_starts_match_oracle(i):
                 first[x] = t
         want = np.array([first[x] if x >= 0 else 2 ** 31 - 1 for x in ids], dtype=np.int64)
         assert np.array_equal(got[b * wl.cp:(b + 1) * wl.cp].reshape(-1).astype(np.int64), want)
+
+
+# plan blob words read below (the layout of block_causal_varlen_gb300/csrc/plan_layout.h)
+_H_NITEMS, _H_OFF_ITEMS, _H_OFF_BWD, _H_NBWD, _H_CK = 13, 14, 19, 20, 23
+_ITEM_WORDS, _I_B, _I_ROW0, _I_SVALID, _I_KVSTART, _I_KVEND, _I_KVBASE = 16, 0, 3, 4, 6, 7, 10
+_BWD_WORDS = 8  # buf, key tile, K/V head, item_lo, item_hi, steps, q_lo, q_hi
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("i", [1, 2, 3, 5])
+def test_plan_backward_units_match_brute_force(i, d):
+    """Every backward work unit (one 128-key tile of a K/V buffer, one K/V head)
+    against a brute force over document ids: its query range is exactly the rows
+    that attend to a key of the tile, and its step count is the number of
+    (query step, query head) pairs that touch those rows, with steps of 128 rows
+    (64 at head dim 256). Every (buffer, tile, head) appears once."""
+    wl = workloads.config(i)
+    G = wl.H // wl.Hkv
+    qstep = 64 if d == 256 else 128
+    for mode in (lib.BD_KV_GATHER, lib.BD_KV_WINDOW):
+        plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, d, kv_mode=mode)
+        h = plan.host
+        items = h[h[_H_OFF_ITEMS]:h[_H_OFF_ITEMS] + h[_H_NITEMS] * _ITEM_WORDS].reshape(-1, _ITEM_WORDS)
+        units = h[h[_H_OFF_BWD]:h[_H_OFF_BWD] + h[_H_NBWD] * _BWD_WORDS].reshape(-1, _BWD_WORDS)
+        ids = [oracle.doc_ids(cu, wl.S) for cu in wl.cu]
+        seen = set()
+        for buf, kt, g, it_lo, it_hi, nq, q_lo, q_hi in units.tolist():
+            assert (buf, kt, g) not in seen
+            seen.add((buf, kt, g))
+            I0 = items[it_lo]
+            b, kv_base, svalid = int(I0[_I_B]), int(I0[_I_KVBASE]), int(I0[_I_SVALID])
+            rows = wl.S if mode == lib.BD_KV_GATHER else int(I0[_I_KVEND] - I0[_I_KVSTART])
+            c0, c1 = kv_base + kt * 128, min(kv_base + kt * 128 + 128, kv_base + rows, svalid)
+            doc = ids[b]
+            attend = np.zeros(wl.S, dtype=bool)
+            for x in sorted(set(doc[c0:c1].tolist()) - {-1}):   # earliest key of each document in the tile
+                jmin = c0 + int(np.argmax(doc[c0:c1] == x))
+                attend |= (doc == x) & (np.arange(wl.S) >= jmin)
+            rows_att = np.flatnonzero(attend)
+            if len(rows_att) == 0:
+                assert nq == 0 and q_lo == q_hi
+                continue
+            assert (q_lo, q_hi) == (int(rows_att[0]), int(rows_att[-1]) + 1)
+            assert len(rows_att) == q_hi - q_lo            # contiguous
+            steps = 0
+            for it in range(it_lo, it_hi):
+                r0 = int(items[it][_I_ROW0])
+                for t in range(-(-wl.L // qstep)):
+                    lo, hi = r0 + t * qstep, min(r0 + (t + 1) * qstep, r0 + wl.L)
+                    steps += bool(attend[lo:hi].any())
+            assert nq == G * steps
+        nbuf = wl.B if mode == lib.BD_KV_GATHER else wl.B * wl.cp
+        assert len(seen) == len(units) and {u[0] for u in seen} <= set(range(nbuf))
+        for nb in range(nbuf):   # every key tile of every buffer, for every K/V head
+            I0 = items[nb * wl.cp if mode == lib.BD_KV_GATHER else nb]
+            rows = wl.S if mode == lib.BD_KV_GATHER else int(I0[_I_KVEND] - I0[_I_KVSTART])
+            want = {(nb, kt, g) for kt in range(-(-rows // 128)) for g in range(wl.Hkv)}
+            assert {u for u in seen if u[0] == nb} == want
