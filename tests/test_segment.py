@@ -263,3 +263,33 @@ def test_plan_backward_units_match_brute_force(i, d):
             rows = wl.S if mode == lib.BD_KV_GATHER else int(I0[_I_KVEND] - I0[_I_KVSTART])
             want = {(nb, kt, g) for kt in range(-(-rows // 128)) for g in range(wl.Hkv)}
             assert {u for u in seen if u[0] == nb} == want
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("i", [1, 2, 3, 4, 5])
+def test_visited_tiles_match_brute_force(i):
+    """The forward visits exactly the 128 x 128 (query tile, key tile) pairs that
+    hold at least one unmasked (row, key): query tiles on each chunk's row grid,
+    key tiles on the global 128-row grid, counted by brute force over every row's
+    key interval [document start, row] (from the document ids)."""
+    wl = workloads.config(i)
+    for mode in (lib.BD_KV_GATHER, lib.BD_KV_WINDOW):
+        plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode)
+        want = 0
+        for b, cu in enumerate(wl.cu):
+            ids = oracle.doc_ids(cu, wl.S)
+            start = np.full(wl.S, -1, dtype=np.int64)
+            for x in range(len(cu) - 1):
+                start[cu[x]:cu[x + 1]] = cu[x]
+            for c in range(wl.cp):
+                for t in range(-(-wl.L // 128)):
+                    lo, hi = c * wl.L + t * 128, min(c * wl.L + (t + 1) * 128, (c + 1) * wl.L)
+                    rows = np.arange(lo, hi)
+                    rows = rows[ids[rows] >= 0]
+                    if len(rows) == 0:
+                        continue
+                    tiles = set()
+                    for r in rows:   # key tiles met by [start(r), r]
+                        tiles.update(range(start[r] // 128, r // 128 + 1))
+                    want += len(tiles)
+        assert plan.fwd_tiles() * plan.slots() == want * wl.H, (i, mode)
