@@ -51,6 +51,30 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def host_info():
+    """CPU model and torch's BLAS, reported with the CPU baseline."""
+    import platform
+    import re
+
+    import torch
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, flags=re.M)
+        model = m.group(1).strip() if m else None
+    except Exception:
+        pass
+    if not model:
+        try:
+            m = re.search(r"^model name\s*:\s*(.+)$", open("/proc/cpuinfo").read(), flags=re.M)
+            model = m.group(1).strip() if m else None
+        except OSError:
+            pass
+    m = re.search(r"BLAS_INFO=([^,\s]+)", torch.__config__.show())
+    return {"cpu_model": model or platform.processor() or platform.machine(), "arch": platform.machine(),
+            "blas": m.group(1) if m else "unknown"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
@@ -260,7 +284,8 @@ def run_reference(args):
             "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "H": wl.H, "Hkv": wl.Hkv,
                        "d": wl.d, "kv_mode": wl.kv_mode},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-                             "sample": "each step: one query chunk x one query head (fwd+bwd), chunks in turn"},
+                             "sample": "each step: one query chunk x one query head (fwd+bwd), chunks in turn",
+                             **host_info()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -478,7 +503,7 @@ def run_ours(args):
             chunks.sort(key=lambda bc: oracle_cost(wl, *bc))
             secs, pairs = oracle_sample(wl, q, k, v, do, chunks, budget_s=12.0, dropout=args.dropout)
             cpu = {"value": 14.0 * wl.d * pairs / secs / 1e12, "unit": "TFLOP/s", "cores": _t.get_num_threads(),
-                   "kind": "oracle", "seconds": secs,
+                   "kind": "oracle", "seconds": secs, **host_info(),
                    "sample": f"oracle fwd+bwd (fp64) on chunks of sequence 0, cheapest first, one K/V head's "
                              f"query heads at a time until ~12 s ({pairs} useful (pair, head) items); "
                              f"TFLOP/s counts the same useful FLOPs"}

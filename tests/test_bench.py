@@ -119,6 +119,7 @@ def test_reference_arm_prints_one_json_line():
         assert key in j, key
     assert j["impl"] == "reference" and j["value"] > 0 and j["steps"] == 2 and j["warmup"] == 1
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
+    assert j["cpu_baseline"]["cpu_model"] and j["cpu_baseline"]["blas"] and j["cpu_baseline"]["cores"] >= 1
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
     assert j["config"]["workload"] == "tiny_s512_3docs_h4_d64_cp2" and j["config"]["d"] == 64
 
