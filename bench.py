@@ -302,6 +302,35 @@ def bench_workload(args):
     return wl
 
 
+def plan_timing(bd, plan, wl, mode, dev, reps=5):
+    """Host build time of the plan (median of `reps` builds) and the time of its
+    one copy to the device (median of `reps` uploads, CUDA events on the current
+    stream): both stay outside the timed step, once per step in training and
+    shared by every layer. None where a measurement could not be taken."""
+    import torch
+    out = {"bytes": int(plan.host.nbytes), "build_ms": None, "upload_ms": None}
+    try:
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode)
+            ts.append(1e3 * (time.perf_counter() - t0))
+        out["build_ms"] = statistics.median(ts)
+        if torch.cuda.is_available():
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                plan.upload(dev)
+                e1.record()
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            out["upload_ms"] = statistics.median(ts)
+    except Exception as e:  # a report field; it never stops the benchmark
+        out["error"] = repr(e)[:200]
+    return out
+
+
 # ------------------------------------------------------------------ our path
 
 def run_ours(args):
@@ -329,6 +358,7 @@ def run_ours(args):
     if args.dropout > 0:
         plan.set_dropout(args.dropout, DROPOUT_SEED)
     plan.upload(dev)
+    plan_cost = plan_timing(bd, plan, wl, mode, dev)
     n_pairs, f_fwd, f_bwd = useful_flops(plan, wl)
     f_step = f_fwd + f_bwd
 
@@ -516,6 +546,7 @@ def run_ours(args):
                        "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
                        "dropout": args.dropout,
                        "tiles": tile_stats(plan, wl),
+                       "plan": plan_cost,
                        "l2": "flushed between steps by a 256 MiB write outside the step events"},
             "fwd_tflops": f_fwd / (t_fwd * 1e-3) / 1e12,
             "bwd_tflops": f_bwd / ((t_pre + t_main + t_own) * 1e-3) / 1e12,

@@ -127,3 +127,13 @@ def test_reference_arm_prints_one_json_line():
 def test_our_arm_refuses_to_run_without_a_gpu():
     r = _run(["--workload", "1", "--steps", "1", "--warmup", "3", "--no-cpu", "--no-e2e"], timeout=300)
     assert r.returncode != 0 and "needs a CUDA GPU" in (r.stderr + r.stdout)
+
+
+def test_plan_timing_reports_build_and_size_on_the_host():
+    lib = pytest.importorskip("block_causal_varlen_gb300")
+    b = _bench()
+    import workloads
+    wl = workloads.config(3)
+    plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=lib.BD_KV_WINDOW)
+    out = b.plan_timing(lib, plan, wl, lib.BD_KV_WINDOW, "cpu", reps=2)
+    assert out["bytes"] == plan.host.nbytes > 0 and out["build_ms"] > 0 and "error" not in out
