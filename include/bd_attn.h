@@ -288,8 +288,8 @@ BD_API int32_t bd_owner_sum_ex(const void* plan_host, const void* plan_dev, cons
 
 /* bd_attn_bwd_noalloc -- bd_attn_bwd for callers that cannot allocate device
  * memory (no allocator is available to them, or a memory cap forbids one
- * more allocation). The paper has no counterpart: it is an addition of this
- * library. The workspace comes from a fixed 16 MiB array in device global
+ * more allocation). The NeMo Automodel page has no counterpart: it is an
+ * addition of this library. The workspace comes from a fixed 16 MiB array in device global
  * memory declared by the library (held on every GPU that loads it until exit);
  * nothing is allocated. Plans needing more workspace than
  * bd_attn_bwd_noalloc_capacity() return BD_ERR_CAPACITY before any launch.
