@@ -137,3 +137,22 @@ def test_plan_timing_reports_build_and_size_on_the_host():
     plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=lib.BD_KV_WINDOW)
     out = b.plan_timing(lib, plan, wl, lib.BD_KV_WINDOW, "cpu", reps=2)
     assert out["bytes"] == plan.host.nbytes > 0 and out["build_ms"] > 0 and "error" not in out
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched like the multi-GPU runs (torchrun, two ranks on 127.0.0.1): rank 0
+    alone prints the JSON line, every rank exits 0."""
+    import socket
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--workload", "1", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["value"] > 0
