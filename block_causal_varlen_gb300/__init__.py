@@ -187,18 +187,25 @@ def _stream(stream):
     return C.c_void_p(stream.cuda_stream)
 
 
-def _need(t, dtype, name):
-    if t.dtype != dtype:
-        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
-    if not t.is_cuda:
-        raise TypeError(f"{name}: must be a CUDA tensor")
+def _check_args(plan: Plan, bf16=(), fp32=(), other=()):
+    """The C ABI carries no dtypes, so the binding checks them (a wrong one would
+    make a kernel read or write past a buffer): bf16 / fp32 tensors as named, every
+    tensor on the plan's device."""
+    for group, dtype in ((bf16, torch.bfloat16), (fp32, torch.float32)):
+        for t, n in group:
+            if t.dtype != dtype:
+                raise TypeError(f"{n}: dtype {t.dtype}, expected {dtype}")
+    dev = plan.dev.device if plan.dev is not None else None
+    for t, n in (*bf16, *fp32, *other):
+        if not t.is_cuda:
+            raise TypeError(f"{n}: must be a CUDA tensor")
+        if dev is not None and t.device != dev:
+            raise ValueError(f"{n}: on {t.device}, the plan was uploaded to {dev}")
 
 
 def bd_attn_fwd(plan: Plan, q, k, v, out, lse, row_offset: int = -1, stream=None):
     """Forward of every chunk item in ``plan`` (see include/bd_attn.h)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
-        _need(t, torch.bfloat16, n)
-    _need(lse, torch.float32, "lse")
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (out, "out")), fp32=((lse, "lse"),))
     tq, tk, tv, to = _tensor(q, "q"), _tensor(k, "k"), _tensor(v, "v"), _tensor(out, "out")
     tl = _rowstat(lse, "lse")
     check(load().bd_attn_fwd(plan.host_ptr, plan.dev_ptr, C.byref(tq), C.byref(tk), C.byref(tv), row_offset,
@@ -214,10 +221,8 @@ def bd_attn_bwd_workspace(plan: Plan) -> int:
 def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accumulate_dkv=False,
                 stream=None):
     """Backward of every chunk item in ``plan`` (see include/bd_attn.h)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
-        _need(t, torch.bfloat16, n)
-    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _need(t, torch.float32, n)
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")),
+                fp32=((lse, "lse"), (dq, "dq"), (dk, "dk"), (dv, "dv")), other=((workspace, "workspace"),))
     ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"))]
     tl = _rowstat(lse, "lse")
     tdq, tdk, tdv = _tensor(dq, "dq"), _tensor(dk, "dk"), _tensor(dv, "dv")
@@ -230,6 +235,8 @@ def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accu
 def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None, clear_dq=True):
     """First backward step only: D, log2 LSE, document starts; zeroes dq unless
     clear_dq is False (the caller then zeroes it before bd_attn_bwd_main)."""
+    _check_args(plan, bf16=((out, "out"), (dout, "dout")), fp32=((lse, "lse"), (dq, "dq")),
+                other=((workspace, "workspace"),))
     to, tg, tq = _tensor(out, "out"), _tensor(dout, "dout"), _tensor(dq, "dq")
     tl = _rowstat(lse, "lse")
     check(load().bd_attn_bwd_pre_ex(plan.host_ptr, plan.dev_ptr, C.byref(to), C.byref(tg), C.byref(tl),
@@ -240,6 +247,8 @@ def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None, clea
 
 def bd_attn_bwd_main(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, accumulate_dkv=False, stream=None):
     """Second backward step only: dq, dk, dv from the workspace bd_attn_bwd_pre filled."""
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (dout, "dout")), fp32=((dq, "dq"), (dk, "dk"), (dv, "dv")),
+                other=((workspace, "workspace"),))
     ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
                                       (dv, "dv"))]
     check(load().bd_attn_bwd_main(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts],
@@ -251,6 +260,7 @@ def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None, accumulate=Tru
     """Sum needed-only-window dK/dV partials at their owner rows, added into dk/dv
     (accumulate=True) or stored there (accumulate=False: every owner row is
     written); see include/bd_attn.h."""
+    _check_args(plan, fp32=((dk_win, "dk_win"), (dv_win, "dv_win"), (dk, "dk"), (dv, "dv")))
     ts = [_tensor(x, n) for x, n in ((dk_win, "dk_win"), (dv_win, "dv_win"), (dk, "dk"), (dv, "dv"))]
     check(load().bd_owner_sum_ex(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], int(bool(accumulate)),
                                  _stream(stream)))

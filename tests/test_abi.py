@@ -58,3 +58,27 @@ def test_padded_len():
     assert lib.bd_padded_len(16381, 4) == 16384
     assert lib.bd_padded_len(16384, 4) == 16384
     assert lib.bd_padded_len(0, 3) == 0
+
+
+def test_binding_checks_dtypes_and_devices_before_the_library():
+    """The C ABI carries no dtypes, so the binding rejects a wrong dtype (which would
+    make a kernel read or write past a buffer) or a host tensor before any call."""
+    import torch
+    bd = pytest.importorskip("block_causal_varlen_gb300")
+    plan = bd.Plan([[0, 200, 350, 512]], 512, 2, 4, 4, 64)
+    bf = torch.zeros(1, 2, 256, 4, 64, dtype=torch.bfloat16)
+    f32 = torch.zeros(1, 2, 256, 4, 64, dtype=torch.float32)
+    kv = torch.zeros(1, 1, 512, 4, 64, dtype=torch.bfloat16)
+    dkv = torch.zeros(1, 1, 512, 4, 64, dtype=torch.float32)
+    lse = torch.zeros(1, 2, 4, 256, dtype=torch.float32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(TypeError, match="dq: dtype"):   # bf16 dq: fp32 reduce-adds would overrun it
+        bd.bd_attn_bwd_main(plan, bf, kv, kv, bf, bf, kv, dkv, ws)
+    with pytest.raises(TypeError, match="dout: dtype"):
+        bd.bd_attn_bwd_pre(plan, bf, f32, lse, f32, ws)
+    with pytest.raises(TypeError, match="dk_win: dtype"):
+        bd.bd_owner_sum(plan, kv, dkv, dkv, dkv)
+    with pytest.raises(TypeError, match="must be a CUDA tensor"):   # right dtypes, host memory
+        bd.bd_attn_bwd(plan, bf, kv, kv, bf, bf, lse, f32, dkv, dkv, ws)
+    with pytest.raises(TypeError, match="must be a CUDA tensor"):
+        bd.bd_attn_fwd(plan, bf, kv, kv, bf, lse)
