@@ -266,6 +266,51 @@ def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None, accumulate=Tru
                                  _stream(stream)))
 
 
+def bd_attn_bwd_pre_ex(plan: Plan, out, dout, lse, dq, workspace, clear_dq: bool, stream=None):
+    """bd_attn_bwd_pre with an explicit clear_dq (the C entry point's form)."""
+    bd_attn_bwd_pre(plan, out, dout, lse, dq, workspace, stream=stream, clear_dq=clear_dq)
+
+
+def bd_owner_sum_ex(plan: Plan, dk_win, dv_win, dk, dv, accumulate: bool, stream=None):
+    """bd_owner_sum with an explicit accumulate (the C entry point's form)."""
+    bd_owner_sum(plan, dk_win, dv_win, dk, dv, stream=stream, accumulate=accumulate)
+
+
+def bd_attn_bwd_noalloc(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, accumulate_dkv=False, stream=None):
+    """bd_attn_bwd with the library's fixed device workspace instead of a caller
+    buffer, for callers that cannot allocate (see include/bd_attn.h)."""
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")),
+                fp32=((lse, "lse"), (dq, "dq"), (dk, "dk"), (dv, "dv")))
+    ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"))]
+    tl = _rowstat(lse, "lse")
+    tdq, tdk, tdv = _tensor(dq, "dq"), _tensor(dk, "dk"), _tensor(dv, "dv")
+    check(load().bd_attn_bwd_noalloc(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], C.byref(tl),
+                                     C.byref(tdq), C.byref(tdk), C.byref(tdv), int(bool(accumulate_dkv)),
+                                     _stream(stream)))
+
+
+def bd_attn_bwd_noalloc_capacity() -> int:
+    """Bytes of the fixed workspace bd_attn_bwd_noalloc draws on."""
+    return int(load().bd_attn_bwd_noalloc_capacity())
+
+
+def bd_padded_len(s: int, cp: int) -> int:
+    """Smallest multiple of cp that is >= s."""
+    n = int(load().bd_padded_len(int(s), int(cp)))
+    check(min(n, 0))
+    return n
+
+
+def bd_version() -> int:
+    return int(load().bd_version())
+
+
+def bd_last_error() -> str:
+    """Message of this thread's last failed call."""
+    m = load().bd_last_error()
+    return m.decode() if m else ""
+
+
 def bd_check_status(plan: Plan, reset: bool = True, stream=None):
     check(load().bd_check_status(plan.dev_ptr, int(reset), _stream(stream)))
 

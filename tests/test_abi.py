@@ -82,3 +82,34 @@ def test_binding_checks_dtypes_and_devices_before_the_library():
         bd.bd_attn_bwd(plan, bf, kv, kv, bf, bf, lse, f32, dkv, dkv, ws)
     with pytest.raises(TypeError, match="must be a CUDA tensor"):
         bd.bd_attn_fwd(plan, bf, kv, kv, bf, lse)
+
+
+# declared entry points the binding serves through the Plan class rather than a
+# module-level function of the same name, and the fault-path self-test
+_VIA_PLAN = {"bd_plan_bytes": "Plan", "bd_plan_build": "Plan", "bd_plan_chunk": "Plan.chunk",
+             "bd_plan_useful_pairs": "Plan.useful_pairs", "bd_plan_set_dropout": "Plan.set_dropout",
+             "bd_selftest_bounded_wait": "tests only"}
+
+
+def test_binding_has_a_function_for_every_declared_entry_point():
+    bd = pytest.importorskip("block_causal_varlen_gb300")
+    for name in _declared():
+        if name in _VIA_PLAN:
+            continue
+        assert callable(getattr(bd, name, None)), f"binding lacks {name}"
+
+
+def test_small_wrappers():
+    import torch
+    bd = pytest.importorskip("block_causal_varlen_gb300")
+    assert bd.bd_padded_len(16381, 4) == 16384 and bd.bd_padded_len(0, 3) == 0
+    with pytest.raises(bd.BDError):
+        bd.bd_padded_len(5, 0)
+    assert "cp" in bd.bd_last_error()
+    assert bd.bd_version() >= 100 and bd.bd_attn_bwd_noalloc_capacity() >= 1 << 20
+    plan = bd.Plan([[0, 200, 350, 512]], 512, 2, 4, 4, 64)
+    bf = torch.zeros(1, 2, 256, 4, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(1, 1, 512, 4, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 4, 256, dtype=torch.float32)
+    with pytest.raises(TypeError, match="dq: dtype"):
+        bd.bd_attn_bwd_noalloc(plan, bf, kv, kv, bf, bf, lse, bf, kv, kv)
