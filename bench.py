@@ -386,17 +386,28 @@ def run_ours(args):
     wsp = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 3 + (1 if mode == bd.BD_KV_WINDOW else 0)  # fwd, bwd pre, bwd main, owner sum
+
+    # needed-only windows over every chunk: dK / dV summed at their owners inside the
+    # backward kernel, and dQ zeroed by the forward's otherwise idle warps
+    fused = (not args.split) and mode == bd.BD_KV_WINDOW and plan.owner_units() > 0
+    launches_per_step = 3 if fused else 3 + (1 if mode == bd.BD_KV_WINDOW else 0)
 
     def step(ev):
         ev[0].record(stream)
-        bd.bd_attn_fwd(plan, qd, kd, vd, out, lse, stream=stream)
+        if fused:
+            bd.bd_attn_fwd_ex(plan, qd, kd, vd, out, lse, dq_zero=dq, stream=stream)
+        else:
+            bd.bd_attn_fwd(plan, qd, kd, vd, out, lse, stream=stream)
         ev[1].record(stream)
-        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, wsp, stream=stream)
+        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, wsp, stream=stream, clear_dq=not fused)
         ev[2].record(stream)
-        bd.bd_attn_bwd_main(plan, qd, kd, vd, dod, dq, dk, dv, wsp, stream=stream)
+        if fused:
+            bd.bd_attn_bwd_main_ex(plan, qd, kd, vd, dod, dq, dk_own, dv_own, wsp, bd.BD_BWD_OWNER_ROWS,
+                                   stream=stream)
+        else:
+            bd.bd_attn_bwd_main(plan, qd, kd, vd, dod, dq, dk, dv, wsp, stream=stream)
         ev[3].record(stream)
-        if mode == bd.BD_KV_WINDOW:  # stores every owner row: nothing to clear between steps
+        if mode == bd.BD_KV_WINDOW and not fused:  # stores every owner row: nothing to clear between steps
             bd.bd_owner_sum(plan, dk, dv, dk_own, dv_own, stream=stream, accumulate=False)
         ev[4].record(stream)
 
@@ -483,11 +494,17 @@ def run_ours(args):
                 in_ready[i].record(s_in)
             stream.wait_event(in_ready[i])
             stream.wait_event(out_done[i])               # step t-2's results have left this set
-            bd.bd_attn_fwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
-            bd.bd_attn_bwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
-                           D_["dvw"], D_["ws"], stream=stream)
-            if mode == bd.BD_KV_WINDOW:
-                bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream, accumulate=False)
+            if fused:
+                bd.bd_attn_fwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], dq_zero=D_["dq"], stream=stream)
+                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dk"],
+                                  D_["dv"], D_["ws"], bd.BD_BWD_OWNER_ROWS | bd.BD_BWD_DQ_ZEROED, stream=stream)
+            else:
+                bd.bd_attn_fwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
+                bd.bd_attn_bwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
+                               D_["dvw"], D_["ws"], stream=stream)
+                if mode == bd.BD_KV_WINDOW:
+                    bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream,
+                                    accumulate=False)
             comp_done[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[i])
@@ -545,6 +562,9 @@ def run_ours(args):
                        "Hkv": wl.Hkv, "d": wl.d, "kv_mode": wl.kv_mode, "layout_seed": wl.seed,
                        "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
                        "dropout": args.dropout,
+                       "path": ("owner-row backward, dQ cleared by the forward" if fused else
+                                "window partials + owner-sum kernel" if mode == bd.BD_KV_WINDOW else
+                                "all-gathered K/V, dK/dV summed in the kernel"),
                        "tiles": tile_stats(plan, wl),
                        "plan": plan_cost,
                        "l2": "flushed between steps by a 256 MiB write outside the step events"},
@@ -555,7 +575,7 @@ def run_ours(args):
             "frac_of_sustained_peak": value / ws / pk["bf16_tflops_sustained"],
             "peak_source": src,
             "kernels_ms": {"bd_fwd_kernel": t_fwd, "bd_bwd_pre_kernel": t_pre, bwd_name: t_main,
-                           "bd_owner_sum_kernel": t_own},
+                           **({} if fused or mode != bd.BD_KV_WINDOW else {"bd_owner_sum_kernel": t_own})},
             "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
                          "peak_source": f"bf16_tflops ({src})"},
@@ -583,6 +603,9 @@ def main():
                     help="attention dropout probability (default 0, as in every benchmarked configuration)")
     ap.add_argument("--head-dim", type=int, default=0, choices=[0, 64, 128, 256],
                     help="replace the workload's head dim (default: keep it)")
+    ap.add_argument("--split", action="store_true",
+                    help="needed-only windows: time window partials + the owner-sum kernel and the statistics "
+                         "kernel clearing dQ, instead of the owner-row backward with dQ cleared by the forward")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -22,12 +22,13 @@ import numpy as np
 import torch
 
 from . import _abi
-from ._abi import (BD_KV_GATHER, BD_KV_WINDOW, BDError, bd_chunk_hdr, bd_rowstat, bd_segment_t,  # noqa: F401
-                   bd_tensor, check, load)
+from ._abi import (BD_BWD_DQ_ZEROED, BD_BWD_OWNER_ROWS, BD_KV_GATHER, BD_KV_WINDOW, BDError,  # noqa: F401
+                   bd_chunk_hdr, bd_rowstat, bd_segment_t, bd_tensor, check, load)
 
-__all__ = ["Plan", "bd_segment", "bd_doc_ids_to_cu", "bd_exchange_plan", "bd_attn_fwd", "bd_attn_bwd", "bd_attn_bwd_pre", "bd_attn_bwd_main",
-           "bd_owner_sum", "bd_check_status",
-           "bd_attn_bwd_workspace", "attn_fwd", "attn_bwd", "BD_KV_GATHER", "BD_KV_WINDOW", "BDError", "load"]
+__all__ = ["Plan", "bd_segment", "bd_doc_ids_to_cu", "bd_exchange_plan", "bd_attn_fwd", "bd_attn_fwd_ex", "bd_attn_bwd",
+           "bd_attn_bwd_ex", "bd_attn_bwd_pre", "bd_attn_bwd_main", "bd_attn_bwd_main_ex", "bd_owner_sum",
+           "bd_check_status", "bd_attn_bwd_workspace", "attn_fwd", "attn_bwd", "BD_KV_GATHER", "BD_KV_WINDOW",
+           "BD_BWD_OWNER_ROWS", "BD_BWD_DQ_ZEROED", "BDError", "load"]
 
 _HDR_FIELDS = ("S", "cp", "rank", "L", "row_offset", "s_valid", "n_pad", "kv_start", "kv_end", "nseg")
 _SEG_FIELDS = ("doc", "q_start", "q_len", "k_start", "k_len", "diag_off")
@@ -145,7 +146,7 @@ class Plan:
         return int(self.host[field])
 
     # index of a few header words (see csrc/plan_layout.h)
-    H_NFWD, H_NBWD, H_KV_ROWS, H_SLOTS, H_FWD_TILES_LO, H_FWD_TILES_HI = 18, 20, 22, 24, 29, 30
+    H_NFWD, H_NBWD, H_KV_ROWS, H_SLOTS, H_FWD_TILES_LO, H_FWD_TILES_HI, H_NBWDO = 18, 20, 22, 24, 29, 30, 37
 
     def slots(self) -> int:
         """Query heads per forward work unit (2 when GQA heads are paired, else 1)."""
@@ -163,6 +164,11 @@ class Plan:
 
     def kv_rows(self) -> int:
         return int(self.host[self.H_KV_ROWS])
+
+    def owner_units(self) -> int:
+        """Backward work units of the plan's owner-keyed list (0 when the plan has
+        none: it needs BD_KV_WINDOW, every chunk 0..cp-1 in order, L % 128 == 0)."""
+        return int(self.host[self.H_NBWDO])
 
 
 def _tensor(t: torch.Tensor, name: str) -> bd_tensor:
@@ -212,6 +218,18 @@ def bd_attn_fwd(plan: Plan, q, k, v, out, lse, row_offset: int = -1, stream=None
                              C.byref(to), C.byref(tl), _stream(stream)))
 
 
+def bd_attn_fwd_ex(plan: Plan, q, k, v, out, lse, dq_zero=None, row_offset: int = -1, stream=None):
+    """bd_attn_fwd that also zeroes ``dq_zero`` (fp32, the backward's dq
+    accumulator) while the forward runs; see include/bd_attn.h."""
+    fp32 = ((lse, "lse"),) + (((dq_zero, "dq_zero"),) if dq_zero is not None else ())
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (out, "out")), fp32=fp32)
+    tq, tk, tv, to = _tensor(q, "q"), _tensor(k, "k"), _tensor(v, "v"), _tensor(out, "out")
+    tl = _rowstat(lse, "lse")
+    tz = C.byref(_tensor(dq_zero, "dq_zero")) if dq_zero is not None else None
+    check(load().bd_attn_fwd_ex(plan.host_ptr, plan.dev_ptr, C.byref(tq), C.byref(tk), C.byref(tv), row_offset,
+                                C.byref(to), C.byref(tl), tz, _stream(stream)))
+
+
 def bd_attn_bwd_workspace(plan: Plan) -> int:
     n = C.c_size_t()
     check(load().bd_attn_bwd_workspace(plan.host_ptr, C.byref(n)))
@@ -230,6 +248,21 @@ def bd_attn_bwd(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, accu
                              C.byref(tdk), C.byref(tdv), int(bool(accumulate_dkv)),
                              C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def bd_attn_bwd_ex(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, workspace, flags: int, accumulate_dkv=False,
+                   stream=None):
+    """bd_attn_bwd with flags: BD_BWD_OWNER_ROWS (dk, dv are owner-row tensors
+    [B, 1, S, Hkv, d] summed over chunks), BD_BWD_DQ_ZEROED (dq already zero)."""
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")),
+                fp32=((lse, "lse"), (dq, "dq"), (dk, "dk"), (dv, "dv")), other=((workspace, "workspace"),))
+    ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"))]
+    tl = _rowstat(lse, "lse")
+    tdq, tdk, tdv = _tensor(dq, "dq"), _tensor(dk, "dk"), _tensor(dv, "dv")
+    check(load().bd_attn_bwd_ex(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], C.byref(tl),
+                                C.byref(tdq), C.byref(tdk), C.byref(tdv), int(bool(accumulate_dkv)), int(flags),
+                                C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
 
 
 def bd_attn_bwd_pre(plan: Plan, out, dout, lse, dq, workspace, stream=None, clear_dq=True):
@@ -254,6 +287,18 @@ def bd_attn_bwd_main(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, accumulat
     check(load().bd_attn_bwd_main(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts],
                                   int(bool(accumulate_dkv)), C.c_void_p(workspace.data_ptr()),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def bd_attn_bwd_main_ex(plan: Plan, q, k, v, dout, dq, dk, dv, workspace, flags: int, accumulate_dkv=False,
+                        stream=None):
+    """bd_attn_bwd_main with flags (BD_BWD_OWNER_ROWS: dk, dv at owner rows)."""
+    _check_args(plan, bf16=((q, "q"), (k, "k"), (v, "v"), (dout, "dout")), fp32=((dq, "dq"), (dk, "dk"), (dv, "dv")),
+                other=((workspace, "workspace"),))
+    ts = [_tensor(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
+                                      (dv, "dv"))]
+    check(load().bd_attn_bwd_main_ex(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts],
+                                     int(bool(accumulate_dkv)), int(flags), C.c_void_p(workspace.data_ptr()),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def bd_owner_sum(plan: Plan, dk_win, dv_win, dk, dv, stream=None, accumulate=True):

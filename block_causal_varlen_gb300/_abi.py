@@ -27,6 +27,9 @@ BD_ERR_PLAN = -10
 BD_KV_GATHER = 0
 BD_KV_WINDOW = 1
 
+BD_BWD_OWNER_ROWS = 1
+BD_BWD_DQ_ZEROED = 2
+
 
 class bd_segment_t(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("doc", "q_start", "q_len", "k_start", "k_len", "diag_off")]
@@ -80,7 +83,19 @@ EXPORTS = {
     "bd_attn_fwd": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                 C.POINTER(bd_tensor), C.c_int32, C.POINTER(bd_tensor), C.POINTER(bd_rowstat),
                                 C.c_void_p]),
+    "bd_attn_fwd_ex": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                   C.POINTER(bd_tensor), C.c_int32, C.POINTER(bd_tensor), C.POINTER(bd_rowstat),
+                                   C.POINTER(bd_tensor), C.c_void_p]),
     "bd_attn_bwd_workspace": (C.c_int32, [C.c_void_p, C.POINTER(C.c_size_t)]),
+    "bd_attn_bwd_ex": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                   C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                   C.POINTER(bd_rowstat), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                   C.POINTER(bd_tensor), C.c_int32, C.c_int32, C.c_void_p, C.c_size_t,
+                                   C.c_void_p]),
+    "bd_attn_bwd_main_ex": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                        C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
+                                        C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.c_int32, C.c_int32,
+                                        C.c_void_p, C.c_size_t, C.c_void_p]),
     "bd_attn_bwd": (C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                 C.POINTER(bd_tensor), C.POINTER(bd_tensor), C.POINTER(bd_tensor),
                                 C.POINTER(bd_rowstat), C.POINTER(bd_tensor), C.POINTER(bd_tensor),

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(512, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t* plan = a.plan;
-  const int32_t* work = plan + plan[H_OFF_BWD];
+  const int32_t* work = plan + a.work_off;
   const int32_t* items = plan + plan[H_OFF_ITEMS];
 
   if (threadIdx.x == 0) {
@@ -143,8 +143,8 @@ __global__ void __launch_bounds__(512, 1)
         if (!(ok = mbar_wait(bar(C_KVEMPTY), (u & 1) ^ 1, abort_flag))) break;
         mbar_expect_tx(bar(C_KVFULL), 2 * Cfg::kTileBytes);
         for (int hf = 0; hf < D / 64; ++hf) {
-          tma_load_5d(sK + hf * 16384, &tm_k, bar(C_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
-          tma_load_5d(sV + hf * 16384, &tm_v, bar(C_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
+          tma_load_5d(sK + hf * 16384, &tm_k, bar(C_KVFULL), hf * 64, g, W[W_LROW], kc, kb);
+          tma_load_5d(sV + hf * 16384, &tm_v, bar(C_KVFULL), hf * 64, g, W[W_LROW], kc, kb);
         }
         ++u;
         const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
@@ -305,8 +305,7 @@ __global__ void __launch_bounds__(512, 1)
       if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
       if (W[W_NQ] == 0) continue;
-      const int32_t* I0 = items + W[W_ITEM_LO] * kItemWords;
-      const int j = I0[I_KVBASE] + W[W_KTILE] * 128 + jl;  // global key row
+      const int j = W[W_KEY0] + jl;  // global key row
       const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
       for (int it = R.it_lo; it < R.it_hi && ok; ++it) {
         int t0, t1, r0;
@@ -363,7 +362,7 @@ __global__ void __launch_bounds__(512, 1)
                 // per 2-query block (word 2 (i mod 2) + (j mod 2) of counter (j/2, i/2, h, b))
                 const int ibase = i0 + ib;
                 uint32_t kb = 0;
-                if ((ibase & 1) == 0 && (I0[I_KVBASE] & 1) == 0) {
+                if ((ibase & 1) == 0 && (W[W_KEY0] & 1) == 0) {
                   // keys 2m, 2m + 1 are lanes 2m, 2m + 1: each lane makes every other
                   // call of the pair and hands its partner the two words it needs
                   const uint32_t odd = lane & 1;
@@ -473,10 +472,10 @@ __global__ void __launch_bounds__(512, 1)
       if (w == -2) ok = false;
       if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
-      const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
-      const int brow = W[W_KTILE] * 128 + rl;  // buffer row of this lane's key
-      float* dkrow = a.dk + kb * a.k_sb + kc * a.k_sc + int64_t(brow) * a.k_sr + int64_t(g) * a.k_sh;
-      float* dvrow = a.dv + kb * a.v_sb + kc * a.v_sc + int64_t(brow) * a.v_sr + int64_t(g) * a.v_sh;
+      const int g = W[W_G], ob = W[W_OBUF] / a.ck_out, oc = W[W_OBUF] % a.ck_out;
+      const int brow = W[W_OROW] + rl;  // output row of this lane's key
+      float* dkrow = a.dk + ob * a.k_sb + oc * a.k_sc + int64_t(brow) * a.k_sr + int64_t(g) * a.k_sh;
+      float* dvrow = a.dv + ob * a.v_sb + oc * a.v_sc + int64_t(brow) * a.v_sr + int64_t(g) * a.v_sh;
       const bool krow_ok = brow < a.dk_rows;
       if (W[W_NQ] == 0) {
         if (krow_ok && !a.accumulate) {
@@ -713,27 +712,41 @@ extern "C" int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, 
   return bd_attn_bwd_pre_ex(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes, 1, stream);
 }
 
-extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, const bd_tensor* q,
-                                    const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
-                                    bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+namespace {
+
+// The main backward kernel over the plan's main work list (dK / dV into the
+// K/V-buffer-shaped dk / dv) or, with owner set, over its owner list (dK / dV
+// of every chunk summed into owner-row tensors [B, 1, S, Hkv, d]).
+int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
+                      const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
+                      int32_t accumulate_dkv, void* workspace, size_t workspace_bytes, void* stream, bool owner,
+                      bool launch = true) {
   BwdCommon c;
   int32_t st = bwd_common(plan_host, plan_dev, workspace, workspace_bytes, &c);
   if (st) return st;
   const PlanView& pv = c.pv;
+  if (owner && pv.hdr(H_NBWDO) == 0)
+    return fail(BD_ERR_UNSUPPORTED,
+                "the plan has no owner-keyed backward work: it needs BD_KV_WINDOW, every chunk 0..cp-1 in "
+                "order and L a multiple of 128");
+  const int ck_out = owner ? 1 : c.Ck;
   if ((st = check_tensor(q, "q", 2, c.B, c.C, c.H, true))) return st;
   if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, true))) return st;
   if ((st = check_tensor(k, "k", 2, c.B, c.Ck, c.Hkv, true))) return st;
   if ((st = check_tensor(v, "v", 2, c.B, c.Ck, c.Hkv, true))) return st;
   if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, true))) return st;
-  if ((st = check_tensor(dk, "dk", 4, c.B, c.Ck, c.Hkv, false))) return st;
-  if ((st = check_tensor(dv, "dv", 4, c.B, c.Ck, c.Hkv, false))) return st;
+  if ((st = check_tensor(dk, "dk", 4, c.B, ck_out, c.Hkv, false))) return st;
+  if ((st = check_tensor(dv, "dv", 4, c.B, ck_out, c.Hkv, false))) return st;
   if (q->rows != c.L || dout->rows != c.L || dq->rows != c.L)
     return fail(BD_ERR_ARG, "q/dout/dq rows must equal L = %d", c.L);
   if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
     return fail(BD_ERR_ARG, "k/v rows < %d needed by the plan", pv.hdr(H_KV_ROWS));
   if (dk->rows != dv->rows) return fail(BD_ERR_ARG, "dk and dv must have the same rows");
-  if (dk->rows < pv.hdr(H_KV_ROWS)) return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
+  if (owner) {
+    if (dk->rows < pv.hdr(H_S)) return fail(BD_ERR_ARG, "owner dk/dv rows must be >= S = %d", pv.hdr(H_S));
+  } else if (dk->rows < pv.hdr(H_KV_ROWS)) {
+    return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
+  }
   CUtensorMap mq, mk, mv, mdo, mdq;
   // dQ reduce boxes: 128 rows x 16 columns (64-byte swizzle), or at head dim 256
   // (transposed dQ) 16 rows x 32 columns (128-byte swizzle); Q / dO boxes are one
@@ -757,14 +770,17 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   a.k_sb = dk->stride_b; a.k_sc = dk->stride_c; a.k_sr = dk->stride_row; a.k_sh = dk->stride_head;
   a.dv = static_cast<float*>(dv->ptr);
   a.v_sb = dv->stride_b; a.v_sc = dv->stride_c; a.v_sr = dv->stride_row; a.v_sh = dv->stride_head;
-  a.L = c.L; a.Lpad = c.Lpad; a.H = c.H; a.G = pv.hdr(H_G); a.Ck = c.Ck; a.n_work = pv.hdr(H_NBWD);
+  a.L = c.L; a.Lpad = c.Lpad; a.H = c.H; a.G = pv.hdr(H_G); a.Ck = c.Ck;
+  a.n_work = owner ? pv.hdr(H_NBWDO) : pv.hdr(H_NBWD);
+  a.work_off = owner ? pv.hdr(H_OFF_BWDO) : pv.hdr(H_OFF_BWD);
+  a.ck_out = ck_out;
   a.accumulate = accumulate_dkv ? 1 : 0; a.dk_rows = dk->rows;
   float scale;
   const int32_t sb = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &sb, 4);
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  if (a.n_work == 0) return ok();
+  if (!launch || a.n_work == 0) return ok();  // validation only, or nothing to do
   int nsm = 0;
   if ((st = sm_count(&nsm))) return st;
   const int grid = a.n_work < nsm ? a.n_work : nsm;
@@ -786,12 +802,54 @@ extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev,
   return ok();
 }
 
+}  // namespace
+
+extern "C" int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                                    const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
+                                    bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return bwd_main_impl(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace, workspace_bytes,
+                       stream, false);
+}
+
+extern "C" int32_t bd_attn_bwd_main_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                                       const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
+                                       bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, int32_t flags,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (flags & ~int32_t(BD_BWD_OWNER_ROWS | BD_BWD_DQ_ZEROED)) return fail(BD_ERR_ARG, "unknown flags 0x%x", flags);
+  return bwd_main_impl(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace, workspace_bytes,
+                       stream, (flags & BD_BWD_OWNER_ROWS) != 0);
+}
+
 extern "C" int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
                                const bd_tensor* v, const bd_tensor* out, const bd_tensor* dout,
                                const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
                                int32_t accumulate_dkv, void* workspace, size_t workspace_bytes, void* stream) {
-  int32_t st = bd_attn_bwd_pre(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes, stream);
+  // the main step's arguments are checked before the statistics kernel runs
+  int32_t st = bwd_main_impl(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace,
+                             workspace_bytes, stream, false, false);
+  if (st) return st;
+  st = bd_attn_bwd_pre(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes, stream);
   if (st) return st;
   return bd_attn_bwd_main(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace,
                           workspace_bytes, stream);
+}
+
+extern "C" int32_t bd_attn_bwd_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                                  const bd_tensor* k, const bd_tensor* v, const bd_tensor* out, const bd_tensor* dout,
+                                  const bd_rowstat* lse, bd_tensor* dq, bd_tensor* dk, bd_tensor* dv,
+                                  int32_t accumulate_dkv, int32_t flags, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (flags & ~int32_t(BD_BWD_OWNER_ROWS | BD_BWD_DQ_ZEROED)) return fail(BD_ERR_ARG, "unknown flags 0x%x", flags);
+  const bool owner = (flags & BD_BWD_OWNER_ROWS) != 0;
+  // the main step's arguments (and, for owner rows, the plan's owner list) are
+  // checked before the statistics kernel runs
+  int32_t st = bwd_main_impl(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace,
+                             workspace_bytes, stream, owner, false);
+  if (st) return st;
+  st = bd_attn_bwd_pre_ex(plan_host, plan_dev, out, dout, lse, dq, workspace, workspace_bytes,
+                          (flags & BD_BWD_DQ_ZEROED) ? 0 : 1, stream);
+  if (st) return st;
+  return bwd_main_impl(plan_host, plan_dev, q, k, v, dout, dq, dk, dv, accumulate_dkv, workspace, workspace_bytes,
+                       stream, owner);
 }

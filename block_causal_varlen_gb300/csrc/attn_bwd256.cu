@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(512, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t* plan = a.plan;
-  const int32_t* work = plan + plan[H_OFF_BWD];
+  const int32_t* work = plan + a.work_off;
   const int32_t* items = plan + plan[H_OFF_ITEMS];
 
   if (threadIdx.x == 0) {
@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(512, 1)
           if (!(ok = mbar_wait(bar(E_KVEMPTY), (u & 1) ^ 1, abort_flag))) break;
           mbar_expect_tx(bar(E_KVFULL), 2 * C::kKVBytes);
           for (int hf = 0; hf < 4; ++hf) {
-            tma_load_5d(sK + hf * 16384, &tm_k, bar(E_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
-            tma_load_5d(sV + hf * 16384, &tm_v, bar(E_KVFULL), hf * 64, g, W[W_KTILE] * 128, kc, kb);
+            tma_load_5d(sK + hf * 16384, &tm_k, bar(E_KVFULL), hf * 64, g, W[W_LROW], kc, kb);
+            tma_load_5d(sV + hf * 16384, &tm_v, bar(E_KVFULL), hf * 64, g, W[W_LROW], kc, kb);
           }
           ++u;
           const StepRange<QR> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
@@ -293,8 +293,7 @@ __global__ void __launch_bounds__(512, 1)
       if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
       if (W[W_NQ] == 0) continue;
-      const int32_t* I0 = items + W[W_ITEM_LO] * kItemWords;
-      const int j = I0[I_KVBASE] + W[W_KTILE] * 128 + jl;  // global key row
+      const int j = W[W_KEY0] + jl;  // global key row
       const StepRange<QR> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
       for (int pass = 0; pass < 2 && ok; ++pass)
         for (int ii = 0; ii < R.it_hi - R.it_lo && ok; ++ii) {
@@ -347,7 +346,7 @@ __global__ void __launch_bounds__(512, 1)
                 // one Philox call per 2-query block (word 2 (i mod 2) + (j mod 2) of
                 // counter (j/2, i/2, h, b))
                 const int ibase = i0 + ib;
-                if ((ibase & 1) == 0 && (I0[I_KVBASE] & 1) == 0) {
+                if ((ibase & 1) == 0 && (W[W_KEY0] & 1) == 0) {
                   // keys 2m, 2m + 1 are lanes 2m, 2m + 1: each lane makes every other
                   // call of the pair and hands its partner the two words it needs
                   const uint32_t odd = lane & 1;
@@ -455,10 +454,10 @@ __global__ void __launch_bounds__(512, 1)
       if (w == -2) ok = false;
       if (w < 0) break;
       const int32_t* W = work + w * kBwdWords;
-      const int g = W[W_G], kb = W[W_BUF] / a.Ck, kc = W[W_BUF] % a.Ck;
-      const int brow = W[W_KTILE] * 128 + rl;  // buffer row of this lane's key
-      float* dkrow = a.dk + kb * a.k_sb + kc * a.k_sc + int64_t(brow) * a.k_sr + int64_t(g) * a.k_sh;
-      float* dvrow = a.dv + kb * a.v_sb + kc * a.v_sc + int64_t(brow) * a.v_sr + int64_t(g) * a.v_sh;
+      const int g = W[W_G], ob = W[W_OBUF] / a.ck_out, oc = W[W_OBUF] % a.ck_out;
+      const int brow = W[W_OROW] + rl;  // output row of this lane's key
+      float* dkrow = a.dk + ob * a.k_sb + oc * a.k_sc + int64_t(brow) * a.k_sr + int64_t(g) * a.k_sh;
+      float* dvrow = a.dv + ob * a.v_sb + oc * a.v_sc + int64_t(brow) * a.v_sr + int64_t(g) * a.v_sh;
       const bool krow_ok = brow < a.dk_rows;
       if (W[W_NQ] == 0) {
         if (krow_ok && !a.accumulate) {

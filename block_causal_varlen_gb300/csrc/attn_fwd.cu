@@ -52,6 +52,11 @@ struct FwdArgs {
   // attention dropout (used by the DROP instantiation): keep iff Philox word >= thresh
   uint32_t drop_thresh, drop_k0, drop_k1;
   float drop_scale;
+  // optional fp32 tensor [B, C, L, H, d] (the backward's dQ accumulator) that the
+  // otherwise idle warps 2-3 set to zero while the forward runs; NULL for none
+  float* dqz;
+  int64_t z_sb, z_sc, z_sr, z_sh;
+  int32_t B, C, H;
 };
 
 template <int D>
@@ -297,22 +302,39 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
    }
-#ifdef BD_TRACE
-   else if ((warp == 2 || warp == 3) && lane == 0 && blockIdx.x == 0) {
-    // tracing build only: stamp the moment each K (warp 2) / V (warp 3) tile lands
-    const bool isk = warp == 2;
-    const int n = isk ? NK : NV;
-    for (uint32_t it = 0; it < uint32_t(kTraceTiles); ++it) {
-      const uint32_t fb = bar((isk ? B_KFULL : B_VFULL) + int(it % n)), par = (it / n) & 1;
-      const uint64_t t0 = globaltimer();
-      bool got = false;
-      while (!(got = mbar_try_wait(fb, par)) && globaltimer() - t0 < 20000000ull) {
+   else {
+    // warps 2-3: zero the caller's dQ accumulator (one d-vector of one (row, head)
+    // per warp store round), spread over every CTA of the launch
+    if (a.dqz != nullptr) {
+      const int64_t nvec = int64_t(a.B) * a.C * a.L * a.H;
+      for (int64_t vid = int64_t(blockIdx.x) * 2 + (warp - 2); vid < nvec; vid += int64_t(gridDim.x) * 2) {
+        const int h = int(vid % a.H);
+        const int64_t r = vid / a.H;
+        const int l = int(r % a.L);
+        const int64_t bc = r / a.L;
+        float* p = a.dqz + (bc / a.C) * a.z_sb + (bc % a.C) * a.z_sc + int64_t(l) * a.z_sr + int64_t(h) * a.z_sh;
+#pragma unroll
+        for (int col = lane * 4; col < D; col += 128)
+          *reinterpret_cast<float4*>(p + col) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (!got) break;
-      BD_TRACE_EVENT(isk ? 26 : 27, int(it));
     }
-   }
+#ifdef BD_TRACE
+    if (lane == 0 && blockIdx.x == 0) {
+      // tracing build only: stamp the moment each K (warp 2) / V (warp 3) tile lands
+      const bool isk = warp == 2;
+      const int n = isk ? NK : NV;
+      for (uint32_t it = 0; it < uint32_t(kTraceTiles); ++it) {
+        const uint32_t fb = bar((isk ? B_KFULL : B_VFULL) + int(it % n)), par = (it / n) & 1;
+        const uint64_t t0 = globaltimer();
+        bool got = false;
+        while (!(got = mbar_try_wait(fb, par)) && globaltimer() - t0 < 20000000ull) {
+        }
+        if (!got) break;
+        BD_TRACE_EVENT(isk ? 26 : 27, int(it));
+      }
+    }
 #endif
+   }
   } else {
     regs_set<Cfg::kRegsSoftmax, Cfg::kRegsLaunch>();
     // ------------------------------------------------------------ softmax
@@ -557,9 +579,9 @@ extern "C" BD_API int32_t bd_trace_read(unsigned long long* host, int32_t cap) {
 }
 #endif
 
-extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
-                               const bd_tensor* v, int32_t row_offset, bd_tensor* out, bd_rowstat* lse,
-                               void* stream) {
+extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                                  const bd_tensor* k, const bd_tensor* v, int32_t row_offset, bd_tensor* out,
+                                  bd_rowstat* lse, bd_tensor* dq_zero, void* stream) {
   PlanView pv;
   int32_t st = view_plan(plan_host, &pv);
   if (st) return st;
@@ -583,6 +605,10 @@ extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, cons
   if (k->rows < pv.hdr(H_KV_ROWS) || v->rows < pv.hdr(H_KV_ROWS))
     return fail(BD_ERR_ARG, "k/v rows %d/%d < %d needed by the plan", k->rows, v->rows, pv.hdr(H_KV_ROWS));
   if (reinterpret_cast<uintptr_t>(lse->ptr) % 4) return fail(BD_ERR_ALIGN, "lse not 4-byte aligned");
+  if (dq_zero) {
+    if ((st = check_tensor(dq_zero, "dq_zero", 4, B, C, H, false))) return st;
+    if (dq_zero->rows != L) return fail(BD_ERR_ARG, "dq_zero rows must equal L = %d", L);
+  }
   CUtensorMap mq, mk, mv;
   if ((st = make_tmap_bf16(&mq, q, B, C, H, D, "q"))) return st;
   if ((st = make_tmap_bf16(&mk, k, B, Ck, Hkv, D, "k"))) return st;
@@ -593,6 +619,10 @@ extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, cons
   a.o_sb = out->stride_b; a.o_sc = out->stride_c; a.o_sr = out->stride_row; a.o_sh = out->stride_head;
   a.lse = lse->ptr; a.l_sb = lse->stride_b; a.l_sc = lse->stride_c; a.l_sh = lse->stride_head;
   a.L = L; a.n_work = pv.hdr(H_NFWD); a.slots = pv.hdr(H_SLOTS); a.Ck = Ck;
+  a.dqz = dq_zero ? static_cast<float*>(dq_zero->ptr) : nullptr;
+  a.z_sb = dq_zero ? dq_zero->stride_b : 0; a.z_sc = dq_zero ? dq_zero->stride_c : 0;
+  a.z_sr = dq_zero ? dq_zero->stride_row : 0; a.z_sh = dq_zero ? dq_zero->stride_head : 0;
+  a.B = B; a.C = C; a.H = H;
   float scale;
   const int32_t scale_bits = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &scale_bits, 4);
@@ -618,4 +648,10 @@ extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, cons
                     : launch_fwd<64, false>(mq, mk, mv, a, grid, s);
   if (st) return st;
   return ok();
+}
+
+extern "C" int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd_tensor* q, const bd_tensor* k,
+                               const bd_tensor* v, int32_t row_offset, bd_tensor* out, bd_rowstat* lse,
+                               void* stream) {
+  return bd_attn_fwd_ex(plan_host, plan_dev, q, k, v, row_offset, out, lse, nullptr, stream);
 }

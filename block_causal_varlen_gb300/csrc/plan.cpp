@@ -57,6 +57,7 @@ int32_t view_plan(const void* plan_host, PlanView* out) {
   };
   if (!in(w[H_OFF_ITEMS], w[H_NITEMS], kItemWords) || !in(w[H_OFF_SEGS], w[H_NSEGS], kSegWords) ||
       !in(w[H_OFF_FWD], w[H_NFWD], kFwdWords) || !in(w[H_OFF_BWD], w[H_NBWD], kBwdWords) ||
+      (w[H_NBWDO] != 0 && !in(w[H_OFF_BWDO], w[H_NBWDO], kBwdWords)) ||
       !in(w[H_OFF_ROWDS], w[H_NITEMS], w[H_L]))
     return fail(BD_ERR_PLAN, "plan blob offsets are inconsistent");
   out->w = w;
@@ -183,7 +184,7 @@ extern "C" int32_t bd_exchange_plan(const int32_t* cu, int32_t ndocs, int32_t S,
 namespace {
 
 struct Built {
-  std::vector<int32_t> items, segs, fwd, bwd, rowds;
+  std::vector<int32_t> items, segs, fwd, bwd, bwdo, rowds;
   int64_t useful = 0, fwd_tiles = 0;
   int32_t kv_rows = 0, slots = 1, qtiles = 0, nbuf = 0, C = 0, Ck = 1;
 };
@@ -301,6 +302,35 @@ int32_t build(const bd_plan_desc* d, Built* out) {
 
   // ---- backward work: (K/V buffer, key tile, K/V head), most query tiles first -------
   struct BW { int32_t w[kBwdWords]; };
+  const int32_t qstep = bwd_query_step(d->d);
+  // query range and (query step) count of the key rows [c0, last] of sequence b over
+  // chunk items [it_lo, it_hi): the rows attending to them are [c0, end of last's document)
+  auto query_span = [&](int32_t b, int32_t it_lo, int32_t it_hi, int32_t c0, int32_t last, int32_t* nq,
+                        int32_t* q_lo, int32_t* q_hi) {
+    *nq = 0;
+    *q_lo = *q_hi = c0;
+    if (last < c0) return;
+    const int32_t* cu = d->cu_seqlens + d->cu_offsets[b];
+    const int32_t nd = d->cu_offsets[b + 1] - d->cu_offsets[b] - 1;
+    const int32_t q_end = *std::upper_bound(cu + 1, cu + nd + 1, last);
+    *q_hi = q_end;
+    for (int32_t it = it_lo; it < it_hi; ++it) {
+      const int32_t* I = &P.items[size_t(it) * kItemWords];
+      const int32_t lo = std::max(c0, I[I_ROW0]), hi = std::min(q_end, I[I_ROW0] + L);
+      if (lo < hi) *nq += (hi - 1 - I[I_ROW0]) / qstep - (lo - I[I_ROW0]) / qstep + 1;
+    }
+  };
+  // CTAs claim units in list order as they finish the previous one, so a list
+  // runs longest first (longest-processing-time order: the last units to start
+  // are the short ones); ties stay grouped by (K/V head, buffer), whose units
+  // read the same Q / dO tiles.
+  auto lpt_order = [](std::vector<BW>& v) {
+    std::stable_sort(v.begin(), v.end(), [](const BW& x, const BW& y) {
+      if (x.w[W_NQ] != y.w[W_NQ]) return x.w[W_NQ] > y.w[W_NQ];
+      if (x.w[W_G] != y.w[W_G]) return x.w[W_G] < y.w[W_G];
+      return x.w[W_OBUF] < y.w[W_OBUF];
+    });
+  };
   std::vector<BW> bw;
   for (int32_t nb = 0; nb < P.nbuf; ++nb) {
     const int32_t b = nb / P.Ck;
@@ -309,40 +339,47 @@ int32_t build(const bd_plan_desc* d, Built* out) {
     const int32_t* I0 = &P.items[size_t(it_lo) * kItemWords];
     const int32_t kv_base = I0[I_KVBASE], svalid = I0[I_SVALID];
     const int32_t rows = d->kv_mode == BD_KV_GATHER ? d->S : I0[I_KVEND] - I0[I_KVSTART];
-    const int32_t* cu = d->cu_seqlens + d->cu_offsets[b];
-    const int32_t nd = d->cu_offsets[b + 1] - d->cu_offsets[b] - 1;
     const int32_t ntiles = (rows + kTile - 1) / kTile;
-    const int32_t qstep = bwd_query_step(d->d);
     for (int32_t kt = 0; kt < ntiles; ++kt) {
       const int32_t c0 = kv_base + kt * kTile;
       const int32_t last = std::min(std::min(c0 + kTile, kv_base + rows), svalid) - 1;
-      int32_t nq = 0, q_lo = c0, q_hi = c0;
-      if (last >= c0) {
-        // queries attending keys [c0, last]: rows [c0, end of last's document)
-        const int32_t* dend = std::upper_bound(cu + 1, cu + nd + 1, last);
-        const int32_t q_end = *dend;
-        q_hi = q_end;
-        for (int32_t it = it_lo; it < it_hi; ++it) {
-          const int32_t* I = &P.items[size_t(it) * kItemWords];
-          const int32_t lo = std::max(c0, I[I_ROW0]), hi = std::min(q_end, I[I_ROW0] + L);
-          if (lo < hi) nq += (hi - 1 - I[I_ROW0]) / qstep - (lo - I[I_ROW0]) / qstep + 1;
-        }
-      }
+      int32_t nq, q_lo, q_hi;
+      query_span(b, it_lo, it_hi, c0, last, &nq, &q_lo, &q_hi);
       for (int32_t g = 0; g < d->Hkv; ++g) {
-        BW w = {{nb, kt, g, it_lo, it_hi, nq * G, q_lo, q_hi}};
+        BW w = {{nb, kt * kTile, g, it_lo, it_hi, nq * G, q_lo, q_hi, c0, nb, kt * kTile, 0}};
         bw.push_back(w);
       }
     }
   }
-  // CTAs claim units in list order as they finish the previous one, so the list
-  // runs longest first (longest-processing-time order: the last units to start
-  // are the short ones); ties stay grouped by (K/V head, buffer), whose units
-  // read the same Q / dO tiles.
-  std::stable_sort(bw.begin(), bw.end(), [](const BW& x, const BW& y) {
-    if (x.w[W_NQ] != y.w[W_NQ]) return x.w[W_NQ] > y.w[W_NQ];
-    if (x.w[W_G] != y.w[W_G]) return x.w[W_G] < y.w[W_G];
-    return x.w[W_BUF] < y.w[W_BUF];
-  });
+  lpt_order(bw);
+  // ---- owner-keyed backward work of a needed-only-window plan over every chunk --------
+  // (sequence, tile of the global 128-row grid, K/V head): the tile lies inside the
+  // rows of one chunk (L % 128 == 0) and so inside that chunk's window, from which
+  // K / V are read; every chunk's query steps add into the same TMEM accumulators
+  // and the sum is stored once at the owner rows.
+  bool all_chunks = C == d->cp;
+  for (int32_t c = 0; all_chunks && c < C; ++c)
+    if (d->ranks && d->ranks[c] != c) all_chunks = false;
+  if (d->kv_mode == BD_KV_WINDOW && all_chunks && L % kTile == 0) {
+    std::vector<BW> bo;
+    for (int32_t b = 0; b < d->B; ++b) {
+      const int32_t svalid = P.items[size_t(b * C) * kItemWords + I_SVALID];
+      for (int32_t kt = 0; kt < d->S / kTile; ++kt) {
+        const int32_t c0 = kt * kTile, c_own = c0 / L, it_own = b * C + c_own;
+        const int32_t* Io = &P.items[size_t(it_own) * kItemWords];
+        const int32_t last = std::min(c0 + kTile, svalid) - 1;
+        int32_t nq, q_lo, q_hi;
+        query_span(b, b * C, (b + 1) * C, c0, last, &nq, &q_lo, &q_hi);
+        const int32_t lrow = last >= c0 ? c0 - Io[I_KVSTART] : 0;
+        for (int32_t g = 0; g < d->Hkv; ++g) {
+          BW w = {{it_own, lrow, g, b * C, (b + 1) * C, nq * G, q_lo, q_hi, c0, b, c0, 0}};
+          bo.push_back(w);
+        }
+      }
+    }
+    lpt_order(bo);
+    for (const BW& w : bo) P.bwdo.insert(P.bwdo.end(), w.w, w.w + kBwdWords);
+  }
   for (const BW& w : bw) P.bwd.insert(P.bwd.end(), w.w, w.w + kBwdWords);
   return BD_OK;
 }
@@ -350,7 +387,7 @@ int32_t build(const bd_plan_desc* d, Built* out) {
 size_t words_of(const Built& P) {
   auto al = [](size_t x) { return (x + 3) & ~size_t(3); };  // keep 16-byte alignment per section
   return kHdrWords + al(P.items.size()) + al(P.segs.size()) + al(P.fwd.size()) + al(P.bwd.size()) +
-         al(P.rowds.size());
+         al(P.bwdo.size()) + al(P.rowds.size());
 }
 
 }  // namespace
@@ -392,6 +429,8 @@ extern "C" int32_t bd_plan_build(const bd_plan_desc* d, void* blob, size_t blob_
   std::copy(P.fwd.begin(), P.fwd.end(), w + off); off += al(P.fwd.size());
   w[H_OFF_BWD] = off; w[H_NBWD] = int32_t(P.bwd.size() / kBwdWords);
   std::copy(P.bwd.begin(), P.bwd.end(), w + off); off += al(P.bwd.size());
+  w[H_OFF_BWDO] = off; w[H_NBWDO] = int32_t(P.bwdo.size() / kBwdWords);
+  std::copy(P.bwdo.begin(), P.bwdo.end(), w + off); off += al(P.bwdo.size());
   w[H_OFF_ROWDS] = off;
   std::copy(P.rowds.begin(), P.rowds.end(), w + off); off += al(P.rowds.size());
   w[H_SCALE_BITS] = scale_bits; w[H_KV_ROWS] = P.kv_rows; w[H_CK] = P.Ck; w[H_SLOTS] = P.slots;

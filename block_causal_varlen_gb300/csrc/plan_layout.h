@@ -22,6 +22,8 @@ enum : int {
   H_DROP_SCALE_BITS,    // 1 / (1 - p) as float bits
   H_DROP_SEED_LO,       // Philox key words
   H_DROP_SEED_HI,
+  H_OFF_BWDO,           // backward work units keyed by owner rows (BD_KV_WINDOW plans
+  H_NBWDO,              // of every chunk in order with L % 128 == 0; else 0 units)
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
   H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
   H_FWD_CLAIM = 58,     // forward work-unit claim counter (0 between launches)
@@ -49,13 +51,24 @@ constexpr int kSegWords = 6;  // doc, q_start, q_len, k_start, k_len, diag_off
 // the global 128-row grid.
 enum : int { F_ITEM = 0, F_QTILE, F_H0, F_KTLO, F_NT, F_PAD0, F_PAD1, F_PAD2, kFwdWords = 8 };
 
-// backward work unit: one 128-row tile of one K/V buffer (buffer rows
-// [128*kt, 128*kt+128)) for one K/V head, visiting the query tiles of chunk
-// items [item_lo, item_hi) that hold global rows in [q_lo, q_hi): the rows
-// that attend to at least one key of the tile (q_lo = q_hi when none).
-// nq counts (query step, query head) pairs; a query step is
-// bwd_query_step(d) rows of one chunk.
-enum : int { W_BUF = 0, W_KTILE, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_QLO, W_QHI, kBwdWords = 8 };
+// backward work unit: one 128-row tile of keys of one K/V head. K and V are
+// read from K/V buffer W_BUF at buffer rows [W_LROW, W_LROW + 128); the tile's
+// first key is global row W_KEY0; its dK / dV rows leave for output buffer
+// W_OBUF at rows [W_OROW, W_OROW + 128). The unit visits the query tiles of
+// chunk items [item_lo, item_hi) that hold global rows in [q_lo, q_hi): the
+// rows that attend to at least one key of the tile (q_lo = q_hi when none).
+// nq counts (query step, query head) pairs; a query step is bwd_query_step(d)
+// rows of one chunk.
+// The plan's main list has one unit per (K/V buffer, 128-row tile of that
+// buffer, K/V head), output = the same buffer and rows. The owner list of a
+// needed-only-window plan has one unit per (sequence, 128-row tile of the
+// global row grid, K/V head): it reads the tile from the window of the chunk
+// that owns those rows and sums every chunk's contribution into the owner
+// rows of a [B, 1, S, Hkv, d] output.
+enum : int {
+  W_BUF = 0, W_LROW, W_G, W_ITEM_LO, W_ITEM_HI, W_NQ, W_QLO, W_QHI, W_KEY0, W_OBUF, W_OROW, W_PAD0,
+  kBwdWords = 12
+};
 
 // Query rows per backward step: 128, and 64 at head dim 256, where a 128-row Q
 // tile and dO tile (64 KB each) would not fit in shared memory next to the

@@ -229,6 +229,18 @@ BD_API int32_t bd_attn_fwd(const void* plan_host, const void* plan_dev, const bd
                     const bd_tensor* k, const bd_tensor* v, int32_t row_offset,
                     bd_tensor* out, bd_rowstat* lse, void* stream);
 
+/* bd_attn_fwd_ex -- bd_attn_fwd that also sets dq_zero, an fp32 query-like
+ * tensor [B, nchunks, L, H, d] (the backward's dq accumulator), to zero while
+ * the forward runs: warps of the forward kernel that have no attention work
+ * store the zeros, so a training step needs no separate clearing pass and the
+ * backward can be told so (BD_BWD_DQ_ZEROED). dq_zero may be NULL (then this is
+ * bd_attn_fwd). It must not alias q, k, v, out or lse. Errors as bd_attn_fwd,
+ * plus BD_ERR_ARG / BD_ERR_ALIGN for a bad dq_zero (rows must equal L). This
+ * clearing is a library addition; the NeMo Automodel page's forward has none. */
+BD_API int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                       const bd_tensor* k, const bd_tensor* v, int32_t row_offset,
+                       bd_tensor* out, bd_rowstat* lse, bd_tensor* dq_zero, void* stream);
+
 /* Workspace bytes bd_attn_bwd needs for this plan (softmax statistics D). */
 BD_API int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes);
 
@@ -246,6 +258,33 @@ BD_API int32_t bd_attn_bwd(const void* plan_host, const void* plan_dev, const bd
                     const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq,
                     bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Flags of bd_attn_bwd_ex / bd_attn_bwd_main_ex. */
+typedef enum {
+  /* dk, dv are owner-row tensors fp32 [B, 1, S', Hkv, d] (S' >= S) instead of
+   * key-like ones: every chunk's contribution to key row r of sequence b is
+   * summed, deterministically, into dk[b, 0, r] -- the reduce-scatter SUM of
+   * the fused all-gather, or the index_add of the needed-only exchange, done in
+   * the kernel (NeMo Automodel page "block-diagonal varlen CP for packed
+   * sequences", Design overview, exchange.py). Rows at or past s_valid get
+   * zeros (with accumulate_dkv = 0). Needs a BD_KV_WINDOW plan over every chunk
+   * 0..cp-1 in order with L a multiple of 128 (else BD_ERR_UNSUPPORTED, before
+   * any launch); k, v are its window buffers. Equal, up to rounding order, to
+   * bd_attn_bwd followed by bd_owner_sum_ex. */
+  BD_BWD_OWNER_ROWS = 1,
+  /* dq is already zero (bd_attn_fwd_ex cleared it): the statistics step skips
+   * clearing it. Ignored by bd_attn_bwd_main_ex. */
+  BD_BWD_DQ_ZEROED = 2
+} bd_bwd_flags;
+
+/* bd_attn_bwd_ex -- bd_attn_bwd with flags (bd_bwd_flags, OR-ed). Every
+ * argument of both steps is checked before the first launch. Unknown flag bits
+ * give BD_ERR_ARG. */
+BD_API int32_t bd_attn_bwd_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                       const bd_tensor* k, const bd_tensor* v, const bd_tensor* out,
+                       const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq,
+                       bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, int32_t flags,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* bd_attn_bwd_pre -- the first step of bd_attn_bwd on its own: per row and
  * head D = <dout, out> (fp32), the LSE in log2 units and each row's document
@@ -268,6 +307,13 @@ BD_API int32_t bd_attn_bwd_main(const void* plan_host, const void* plan_dev, con
                          const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
                          bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/* bd_attn_bwd_main_ex -- bd_attn_bwd_main with flags: BD_BWD_OWNER_ROWS sums
+ * dk / dv at their owner rows (see bd_bwd_flags). */
+BD_API int32_t bd_attn_bwd_main_ex(const void* plan_host, const void* plan_dev, const bd_tensor* q,
+                            const bd_tensor* k, const bd_tensor* v, const bd_tensor* dout, bd_tensor* dq,
+                            bd_tensor* dk, bd_tensor* dv, int32_t accumulate_dkv, int32_t flags,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* bd_owner_sum -- add the BD_KV_WINDOW partials dk_win/dv_win (key-like fp32,
  * Ck = nchunks) of every chunk of the plan into owner-row tensors dk/dv

@@ -99,3 +99,22 @@ def o_check(got, want):
     err_rel = max_rel(got, want)
     assert math.isfinite(err_abs) and err_abs <= O_ABS and err_rel <= O_REL, (err_abs, err_rel)
     return err_abs, err_rel
+
+
+def doc_rel(x, ref, cu, floor=1e-2):
+    """Largest per-document max-rel over the documents of one sequence: rows
+    [cu[k], cu[k+1]) of x / ref (dim 0 = row), each normalised by that document's
+    own max|ref|, floored at `floor` x the whole tensor's max|ref| (a document whose
+    exact values are ~0, e.g. dK of a one-token document, is judged against that
+    floor instead of its own rounding noise)."""
+    x = x.double()
+    ref = ref.double()
+    top = ref.abs().max().item()
+    worst = 0.0
+    for a, e in zip(cu[:-1], cu[1:]):
+        if e <= a:
+            continue
+        den = max(ref[a:e].abs().max().item(), floor * top)
+        if den > 0:
+            worst = max(worst, (x[a:e] - ref[a:e]).abs().max().item() / den)
+    return worst

@@ -207,9 +207,38 @@ def test_plan_row_doc_starts_match_oracle(i):
 
 
 # plan blob words read below (the layout of block_causal_varlen_gb300/csrc/plan_layout.h)
-_H_NITEMS, _H_OFF_ITEMS, _H_OFF_BWD, _H_NBWD, _H_CK = 13, 14, 19, 20, 23
+_H_NITEMS, _H_OFF_ITEMS, _H_OFF_BWD, _H_NBWD, _H_CK, _H_OFF_BWDO, _H_NBWDO = 13, 14, 19, 20, 23, 36, 37
 _ITEM_WORDS, _I_B, _I_ROW0, _I_SVALID, _I_KVSTART, _I_KVEND, _I_KVBASE = 16, 0, 3, 4, 6, 7, 10
-_BWD_WORDS = 8  # buf, key tile, K/V head, item_lo, item_hi, steps, q_lo, q_hi
+# load buffer, load row, K/V head, item_lo, item_hi, steps, q_lo, q_hi, first key row, output buffer,
+# output row, pad
+_BWD_WORDS = 12
+
+
+def _check_unit_queries(wl, items, doc, it_lo, it_hi, c0, c1, nq, q_lo, q_hi, qstep):
+    """The unit's query range is exactly the rows attending to a key in [c0, c1)
+    and its step count the (query step, query head) pairs that touch them."""
+    G = wl.H // wl.Hkv
+    attend = np.zeros(wl.S, dtype=bool)
+    for x in sorted(set(doc[c0:c1].tolist()) - {-1}):   # earliest key of each document in the tile
+        jmin = c0 + int(np.argmax(doc[c0:c1] == x))
+        attend |= (doc == x) & (np.arange(wl.S) >= jmin)
+    rows_att = np.flatnonzero(attend)
+    if len(rows_att) == 0:
+        assert nq == 0 and q_lo == q_hi
+        return
+    assert (q_lo, q_hi) == (int(rows_att[0]), int(rows_att[-1]) + 1)
+    assert len(rows_att) == q_hi - q_lo            # contiguous
+    steps = 0
+    for it in range(it_lo, it_hi):
+        r0 = int(items[it][_I_ROW0])
+        for t in range(-(-wl.L // qstep)):
+            lo, hi = r0 + t * qstep, min(r0 + (t + 1) * qstep, r0 + wl.L)
+            steps += bool(attend[lo:hi].any())
+    assert nq == G * steps
+
+
+def _units(h, off, n):
+    return h[h[off]:h[off] + h[n] * _BWD_WORDS].reshape(-1, _BWD_WORDS)
 
 
 @pytestmark_lib
@@ -220,42 +249,28 @@ def test_plan_backward_units_match_brute_force(i, d):
     against a brute force over document ids: its query range is exactly the rows
     that attend to a key of the tile, and its step count is the number of
     (query step, query head) pairs that touch those rows, with steps of 128 rows
-    (64 at head dim 256). Every (buffer, tile, head) appears once."""
+    (64 at head dim 256). Every (buffer, tile, head) appears once, and its dK / dV
+    rows go back to the same buffer rows."""
     wl = workloads.config(i)
-    G = wl.H // wl.Hkv
     qstep = 64 if d == 256 else 128
     for mode in (lib.BD_KV_GATHER, lib.BD_KV_WINDOW):
         plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, d, kv_mode=mode)
         h = plan.host
         items = h[h[_H_OFF_ITEMS]:h[_H_OFF_ITEMS] + h[_H_NITEMS] * _ITEM_WORDS].reshape(-1, _ITEM_WORDS)
-        units = h[h[_H_OFF_BWD]:h[_H_OFF_BWD] + h[_H_NBWD] * _BWD_WORDS].reshape(-1, _BWD_WORDS)
+        units = _units(h, _H_OFF_BWD, _H_NBWD)
         ids = [oracle.doc_ids(cu, wl.S) for cu in wl.cu]
         seen = set()
-        for buf, kt, g, it_lo, it_hi, nq, q_lo, q_hi in units.tolist():
+        for buf, lrow, g, it_lo, it_hi, nq, q_lo, q_hi, key0, obuf, orow, _ in units.tolist():
+            assert lrow % 128 == 0 and (obuf, orow) == (buf, lrow)
+            kt = lrow // 128
             assert (buf, kt, g) not in seen
             seen.add((buf, kt, g))
             I0 = items[it_lo]
             b, kv_base, svalid = int(I0[_I_B]), int(I0[_I_KVBASE]), int(I0[_I_SVALID])
+            assert key0 == kv_base + lrow
             rows = wl.S if mode == lib.BD_KV_GATHER else int(I0[_I_KVEND] - I0[_I_KVSTART])
             c0, c1 = kv_base + kt * 128, min(kv_base + kt * 128 + 128, kv_base + rows, svalid)
-            doc = ids[b]
-            attend = np.zeros(wl.S, dtype=bool)
-            for x in sorted(set(doc[c0:c1].tolist()) - {-1}):   # earliest key of each document in the tile
-                jmin = c0 + int(np.argmax(doc[c0:c1] == x))
-                attend |= (doc == x) & (np.arange(wl.S) >= jmin)
-            rows_att = np.flatnonzero(attend)
-            if len(rows_att) == 0:
-                assert nq == 0 and q_lo == q_hi
-                continue
-            assert (q_lo, q_hi) == (int(rows_att[0]), int(rows_att[-1]) + 1)
-            assert len(rows_att) == q_hi - q_lo            # contiguous
-            steps = 0
-            for it in range(it_lo, it_hi):
-                r0 = int(items[it][_I_ROW0])
-                for t in range(-(-wl.L // qstep)):
-                    lo, hi = r0 + t * qstep, min(r0 + (t + 1) * qstep, r0 + wl.L)
-                    steps += bool(attend[lo:hi].any())
-            assert nq == G * steps
+            _check_unit_queries(wl, items, ids[b], it_lo, it_hi, c0, c1, nq, q_lo, q_hi, qstep)
         nbuf = wl.B if mode == lib.BD_KV_GATHER else wl.B * wl.cp
         assert len(seen) == len(units) and {u[0] for u in seen} <= set(range(nbuf))
         for nb in range(nbuf):   # every key tile of every buffer, for every K/V head
@@ -263,6 +278,60 @@ def test_plan_backward_units_match_brute_force(i, d):
             rows = wl.S if mode == lib.BD_KV_GATHER else int(I0[_I_KVEND] - I0[_I_KVSTART])
             want = {(nb, kt, g) for kt in range(-(-rows // 128)) for g in range(wl.Hkv)}
             assert {u for u in seen if u[0] == nb} == want
+        # the owner-keyed list exists for needed-only windows over every chunk (L % 128 == 0 here)
+        assert (plan.owner_units() > 0) == (mode == lib.BD_KV_WINDOW)
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("i", [1, 2, 3, 5])
+def test_plan_owner_units_match_brute_force(i, d):
+    """The owner-keyed backward list of a needed-only-window plan: one unit per
+    (sequence, 128-row tile of the global row grid, K/V head), every one exactly
+    once; K / V come from the window of the chunk that owns the tile, at the rows
+    that hold the tile's global rows; every chunk of the sequence contributes and
+    the result goes to the owner rows; the query range and step count match the
+    brute force over document ids."""
+    wl = workloads.config(i)
+    qstep = 64 if d == 256 else 128
+    plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, d, kv_mode=lib.BD_KV_WINDOW)
+    h = plan.host
+    items = h[h[_H_OFF_ITEMS]:h[_H_OFF_ITEMS] + h[_H_NITEMS] * _ITEM_WORDS].reshape(-1, _ITEM_WORDS)
+    units = _units(h, _H_OFF_BWDO, _H_NBWDO)
+    assert len(units) == wl.B * (wl.S // 128) * wl.Hkv
+    ids = [oracle.doc_ids(cu, wl.S) for cu in wl.cu]
+    seen = set()
+    for buf, lrow, g, it_lo, it_hi, nq, q_lo, q_hi, key0, obuf, orow, _ in units.tolist():
+        b = obuf
+        assert (it_lo, it_hi) == (b * wl.cp, (b + 1) * wl.cp)
+        assert orow == key0 and key0 % 128 == 0
+        assert (b, key0, g) not in seen
+        seen.add((b, key0, g))
+        own = b * wl.cp + key0 // wl.L
+        assert buf == own
+        svalid = int(items[own][_I_SVALID])
+        c1 = min(key0 + 128, svalid)
+        if c1 > key0:   # the owner's window holds the tile's valid rows at lrow..
+            kvs, kve = int(items[own][_I_KVSTART]), int(items[own][_I_KVEND])
+            assert lrow == key0 - kvs and kvs <= key0 and c1 <= kve
+        _check_unit_queries(wl, items, ids[b], it_lo, it_hi, key0, max(c1, key0), nq, q_lo, q_hi, qstep)
+    assert seen == {(b, kt * 128, g) for b in range(wl.B) for kt in range(wl.S // 128) for g in range(wl.Hkv)}
+    # the same work as the per-window list, tile by tile (both count every attending
+    # (query step, head) pair of every chunk once per key tile of their own grids)
+    steps_owner = int(units[:, 5].sum())
+    assert steps_owner > 0
+
+
+@pytestmark_lib
+def test_owner_units_only_for_whole_window_plans():
+    """No owner list (the owner-row backward refuses the plan) for all-gathered K/V,
+    a subset of the chunks, or L not a multiple of 128."""
+    cu = [[0, 300, 700, 1000]]
+    assert lib.Plan(cu, 1024, 4, 4, 4, 64, kv_mode=lib.BD_KV_WINDOW).owner_units() == 8 * 4  # L = 256
+    assert lib.Plan(cu, 1024, 2, 4, 4, 64, kv_mode=lib.BD_KV_WINDOW).owner_units() > 0     # L = 512
+    assert lib.Plan(cu, 1024, 2, 4, 4, 64, kv_mode=lib.BD_KV_GATHER).owner_units() == 0
+    assert lib.Plan(cu, 1024, 2, 4, 4, 64, kv_mode=lib.BD_KV_WINDOW, ranks=[1]).owner_units() == 0
+    assert lib.Plan(cu, 1200, 4, 4, 4, 64, kv_mode=lib.BD_KV_WINDOW).owner_units() == 0   # L = 300
 
 
 @pytestmark_lib
