@@ -97,7 +97,7 @@ class Clocks:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -209,12 +209,14 @@ def useful_flops(plan, wl):
 DROPOUT_SEED = 0x5EED0F0D0F0A77E0  # fixed seed of the --dropout runs
 
 
-def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None, dropout=0.0):
+def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None, dropout=0.0, dtype=None):
     """Time the oracle (fwd + bwd) on the host cores over the given chunks, one
     K/V head's query heads at a time (heads: how many query heads; with budget_s,
-    stop once that many seconds have been spent, after at least one group).
-    Returns (seconds, useful (pair, head) items)."""
+    stop once that many seconds have been spent, after at least one group), in
+    ``dtype`` (default fp32, the precision the oracle is specified in; the tests
+    run it in fp64). Returns (seconds, useful (pair, head) items)."""
     import torch
+    dtype = torch.float32 if dtype is None else dtype
 
     import oracle
     G = wl.H // wl.Hkv
@@ -234,12 +236,13 @@ def oracle_sample(wl, q, k, v, do, chunks, heads=None, budget_s=None, dropout=0.
             if dropout > 0:
                 # the head index only selects the keep mask; timing is what matters here
                 oracle.chunk_fwd_dropout(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, dropout, DROPOUT_SEED,
-                                         b=b, kv_base=a)
+                                         b=b, kv_base=a, dtype=dtype)
                 oracle.chunk_bwd_dropout(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L,
-                                         dropout, DROPOUT_SEED, b=b, kv_base=a)
+                                         dropout, DROPOUT_SEED, b=b, kv_base=a, dtype=dtype)
             else:
-                oracle.chunk_fwd(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, kv_base=a)
-                oracle.chunk_bwd(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L, kv_base=a)
+                oracle.chunk_fwd(q[b, rows, hq], kw, vw, wl.cu[b], wl.S, c * wl.L, kv_base=a, dtype=dtype)
+                oracle.chunk_bwd(q[b, rows, hq], kw, vw, do[b, rows, hq], wl.cu[b], wl.S, c * wl.L, kv_base=a,
+                                 dtype=dtype)
             pairs += n_chunk * (hq.stop - hq.start)
             if budget_s is not None and time.perf_counter() - t0 > budget_s:
                 done = True
@@ -271,7 +274,8 @@ def run_reference(args):
     chunks_all = [(b, c) for b in range(wl.B) for c in range(wl.cp) if wl.cu[b][-1] > c * wl.L]
     times, pairs = [], []
     for s in range(args.warmup + args.steps):
-        t, p = oracle_sample(wl, q, k, v, do, [chunks_all[s % len(chunks_all)]], heads=1, budget_s=0.0)
+        t, p = oracle_sample(wl, q, k, v, do, [chunks_all[s % len(chunks_all)]], heads=1, budget_s=0.0,
+                             dtype=torch.float32)
         if s >= args.warmup:
             times.append(t)
             pairs.append(p)
@@ -279,12 +283,13 @@ def run_reference(args):
     value = flops / sum(times) / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "H": wl.H, "Hkv": wl.Hkv,
                        "d": wl.d, "kv_mode": wl.kv_mode},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-                             "sample": "each step: one query chunk x one query head (fwd+bwd), chunks in turn",
+                             "dtype": "f32",
+                             "sample": "each step: one query chunk x one query head (fwd+bwd, fp32), chunks in turn",
                              **host_info()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -332,6 +337,77 @@ def plan_timing(bd, plan, wl, mode, dev, reps=5):
 
 
 # ------------------------------------------------------------------ our path
+
+def workloads_block(bd, dev, flush, steps=20, warmup=3):
+    """Every other workload (and head dim 256 on the 16k layout) timed the same
+    way as the headline: inputs resident, L2 flushed between steps outside the
+    events, median of `steps` steps; forward alone and forward + backward."""
+    import dataclasses
+
+    import torch
+
+    import workloads
+    cases = [(1, 0), (2, 0), (4, 0), (5, 0), (3, 256)]
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for i, hd in cases:
+        wl = workloads.config(i)
+        if hd:
+            wl = dataclasses.replace(wl, d=hd, name=wl.name.replace(f"_d{wl.d}", f"_d{hd}"))
+        mode = bd.BD_KV_WINDOW if wl.kv_mode == "window" else bd.BD_KV_GATHER
+        plan = bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode).upload(dev)
+        fused = mode == bd.BD_KV_WINDOW and plan.owner_units() > 0
+        q, k, v, do = workloads.tensors(wl)
+        qd = q.to(dev).view(wl.B, wl.cp, wl.L, wl.H, wl.d)
+        dod = do.to(dev).view_as(qd)
+        del q, do
+        if mode == bd.BD_KV_WINDOW:
+            W = plan.kv_rows()
+            kd = torch.zeros(wl.B, wl.cp, W, wl.Hkv, wl.d, dtype=torch.bfloat16, device=dev)
+            vd = torch.zeros_like(kd)
+            for b in range(wl.B):
+                for c in range(wl.cp):
+                    hdr, _ = plan.chunk(b * wl.cp + c)
+                    a, e = hdr["kv_start"], hdr["kv_end"]
+                    kd[b, c, :e - a] = k[b, a:e].to(dev)
+                    vd[b, c, :e - a] = v[b, a:e].to(dev)
+        else:
+            kd, vd = k.to(dev).unsqueeze(1), v.to(dev).unsqueeze(1)
+        del k, v
+        out_t = torch.empty_like(qd)
+        lse = torch.empty(wl.B, wl.cp, wl.H, wl.L, dtype=torch.float32, device=dev)
+        dq = torch.empty(qd.shape, dtype=torch.float32, device=dev)
+        gshape = (wl.B, 1, wl.S, wl.Hkv, wl.d) if fused else kd.shape
+        dk = torch.empty(gshape, dtype=torch.float32, device=dev)
+        dv = torch.empty_like(dk)
+        wsp = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device=dev)
+        flags = bd.BD_BWD_OWNER_ROWS if fused else 0
+        n_pairs, f_fwd, f_bwd = useful_flops(plan, wl)
+
+        def one(with_bwd):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            flush.zero_()
+            ev[0].record(stream)
+            bd.bd_attn_fwd(plan, qd, kd, vd, out_t, lse, stream=stream)
+            ev[1].record(stream)
+            if with_bwd:
+                bd.bd_attn_bwd_ex(plan, qd, kd, vd, out_t, dod, lse, dq, dk, dv, wsp, flags, stream=stream)
+            ev[2].record(stream)
+            return ev
+
+        evs = [one(True) for _ in range(warmup + steps)][warmup:]
+        torch.cuda.synchronize(dev)
+        bd.bd_check_status(plan)
+        t_f = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+        t_s = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+        out[wl.name] = {"fwd_ms": t_f, "fwd_bwd_ms": t_s, "fwd_tflops": f_fwd / (t_f * 1e-3) / 1e12,
+                        "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_s * 1e-3) / 1e12, "useful_pairs": n_pairs,
+                        "kv_mode": wl.kv_mode, "path": "owner-row backward" if fused else "backward",
+                        "steps": steps}
+        del qd, dod, kd, vd, out_t, lse, dq, dk, dv, wsp, plan
+        torch.cuda.empty_cache()
+    return out
+
 
 def run_ours(args):
     import torch
@@ -388,18 +464,20 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     # needed-only windows over every chunk: dK / dV summed at their owners inside the
-    # backward kernel, and dQ zeroed by the forward's otherwise idle warps
+    # backward kernel (no owner-sum kernel); --dq-in-fwd also moves the zeroing of dQ
+    # from the statistics kernel to the forward's otherwise idle warps
     fused = (not args.split) and mode == bd.BD_KV_WINDOW and plan.owner_units() > 0
+    zero_in_fwd = args.dq_in_fwd
     launches_per_step = 3 if fused else 3 + (1 if mode == bd.BD_KV_WINDOW else 0)
 
     def step(ev):
         ev[0].record(stream)
-        if fused:
+        if zero_in_fwd:
             bd.bd_attn_fwd_ex(plan, qd, kd, vd, out, lse, dq_zero=dq, stream=stream)
         else:
             bd.bd_attn_fwd(plan, qd, kd, vd, out, lse, stream=stream)
         ev[1].record(stream)
-        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, wsp, stream=stream, clear_dq=not fused)
+        bd.bd_attn_bwd_pre(plan, out, dod, lse, dq, wsp, stream=stream, clear_dq=not zero_in_fwd)
         ev[2].record(stream)
         if fused:
             bd.bd_attn_bwd_main_ex(plan, qd, kd, vd, dod, dq, dk_own, dv_own, wsp, bd.BD_BWD_OWNER_ROWS,
@@ -441,11 +519,13 @@ def run_ours(args):
         torch.distributed.barrier()
     bd.bd_check_status(plan)
     seg = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]  # ms
-    t_fwd = sum(x[0] for x in seg) / args.steps
-    t_pre = sum(x[1] for x in seg) / args.steps
-    t_main = sum(x[2] for x in seg) / args.steps
-    t_own = sum(x[3] for x in seg) / args.steps
-    t_step = sum(sum(x) for x in seg) / args.steps
+    # medians over the timed steps (the mean is reported beside the step time)
+    t_fwd = statistics.median(x[0] for x in seg)
+    t_pre = statistics.median(x[1] for x in seg)
+    t_main = statistics.median(x[2] for x in seg)
+    t_own = statistics.median(x[3] for x in seg)
+    t_step = statistics.median(sum(x) for x in seg)
+    t_step_mean = sum(sum(x) for x in seg) / args.steps
     if ws > 1:
         tt = torch.tensor([t_step], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -474,7 +554,9 @@ def run_ours(args):
                         dk=torch.zeros_like(dk_own), dv=torch.zeros_like(dv_own),
                         ws=torch.empty_like(wsp))
             sets.append(dset)
-        h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
+        # the plan blob goes up once per step too (host build stays outside: it is the same blob every step)
+        plan_pinned = torch.from_numpy(plan.host).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in[0].values()) + plan_pinned.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         in_ready = [torch.cuda.Event() for _ in range(2)]
@@ -494,14 +576,18 @@ def run_ours(args):
                 in_ready[i].record(s_in)
             stream.wait_event(in_ready[i])
             stream.wait_event(out_done[i])               # step t-2's results have left this set
-            if fused:
+            plan.dev.copy_(plan_pinned, non_blocking=True)  # on the compute stream: after the last step's kernels
+            if zero_in_fwd:
                 bd.bd_attn_fwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], dq_zero=D_["dq"], stream=stream)
-                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dk"],
-                                  D_["dv"], D_["ws"], bd.BD_BWD_OWNER_ROWS | bd.BD_BWD_DQ_ZEROED, stream=stream)
             else:
                 bd.bd_attn_fwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
-                bd.bd_attn_bwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
-                               D_["dvw"], D_["ws"], stream=stream)
+            zflag = bd.BD_BWD_DQ_ZEROED if zero_in_fwd else 0
+            if fused:
+                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dk"],
+                                  D_["dv"], D_["ws"], bd.BD_BWD_OWNER_ROWS | zflag, stream=stream)
+            else:
+                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
+                                  D_["dvw"], D_["ws"], zflag, stream=stream)
                 if mode == bd.BD_KV_WINDOW:
                     bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream,
                                     accumulate=False)
@@ -529,7 +615,13 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "pipeline": "double-buffered: next step's H2D and previous step's D2H overlap this step's kernels"}
 
+    others = None
+    if not args.no_workloads and ws == 1:
+        others = workloads_block(bd, dev, flush)
     pk, src = peaks()
+    if others:
+        for rec in others.values():
+            rec["frac_of_peak"] = rec["fwd_bwd_tflops"] / pk["bf16_tflops"]
     bwd_name = "bd_bwd256_kernel" if wl.d == 256 else "bd_bwd_kernel"  # head dim 256 has its own kernel
     dominant = bwd_name if t_main >= t_fwd else "bd_fwd_kernel"
     dom_ms = t_main if dominant == bwd_name else t_fwd
@@ -548,23 +640,32 @@ def run_ours(args):
             chunks = [(b0, c) for c in range(wl.cp) if wl.cu[b0][-1] > c * wl.L]
             # cheapest chunks first, one K/V head's query heads at a time, until ~12 s of oracle work
             chunks.sort(key=lambda bc: oracle_cost(wl, *bc))
-            secs, pairs = oracle_sample(wl, q, k, v, do, chunks, budget_s=12.0, dropout=args.dropout)
-            cpu = {"value": 14.0 * wl.d * pairs / secs / 1e12, "unit": "TFLOP/s", "cores": _t.get_num_threads(),
-                   "kind": "oracle", "seconds": secs, **host_info(),
-                   "sample": f"oracle fwd+bwd (fp64) on chunks of sequence 0, cheapest first, one K/V head's "
-                             f"query heads at a time until ~12 s ({pairs} useful (pair, head) items); "
-                             f"TFLOP/s counts the same useful FLOPs"}
+            secs, pairs = oracle_sample(wl, q, k, v, do, chunks, budget_s=10.0, dropout=args.dropout)
+            secs64, pairs64 = oracle_sample(wl, q, k, v, do, chunks, budget_s=5.0, dropout=args.dropout,
+                                            dtype=_t.float64)
+            v32 = 14.0 * wl.d * pairs / secs / 1e12
+            v64 = 14.0 * wl.d * pairs64 / secs64 / 1e12
+            cpu = {"value": v32, "unit": "TFLOP/s", "cores": _t.get_num_threads(),
+                   "kind": "oracle", "seconds": secs, "dtype": "f32", **host_info(),
+                   "fp64": {"value": v64, "seconds": secs64, "pairs": pairs64, "fp32_over_fp64": v32 / v64},
+                   "sample": f"oracle fwd+bwd in fp32 (the precision the oracle is specified in) on chunks of "
+                             f"sequence 0, cheapest first, one K/V head's query heads at a time until ~10 s "
+                             f"({pairs} useful (pair, head) items); the same in fp64 (the tests' precision) for "
+                             f"~5 s; TFLOP/s counts the same useful FLOPs"}
         result = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": t_step, "ms_per_step_mean": t_step_mean,
+            "step_statistic": "median of the timed steps' CUDA-event intervals",
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "cp": wl.cp, "L": wl.L, "H": wl.H,
                        "Hkv": wl.Hkv, "d": wl.d, "kv_mode": wl.kv_mode, "layout_seed": wl.seed,
                        "useful_pairs": n_pairs, "useful_flops_fwd": f_fwd, "useful_flops_bwd": f_bwd,
                        "dropout": args.dropout,
-                       "path": ("owner-row backward, dQ cleared by the forward" if fused else
+                       "path": ("owner-row backward" if fused else
                                 "window partials + owner-sum kernel" if mode == bd.BD_KV_WINDOW else
-                                "all-gathered K/V, dK/dV summed in the kernel"),
+                                "all-gathered K/V, dK/dV summed in the kernel")
+                               + ("; dQ zeroed by the forward" if zero_in_fwd else "; dQ zeroed by the statistics kernel"),
                        "tiles": tile_stats(plan, wl),
                        "plan": plan_cost,
                        "l2": "flushed between steps by a 256 MiB write outside the step events"},
@@ -581,6 +682,7 @@ def run_ours(args):
                          "peak_source": f"bf16_tflops ({src})"},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "workloads": others,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
@@ -603,6 +705,11 @@ def main():
                     help="attention dropout probability (default 0, as in every benchmarked configuration)")
     ap.add_argument("--head-dim", type=int, default=0, choices=[0, 64, 128, 256],
                     help="replace the workload's head dim (default: keep it)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload block (the other workloads and head dim 256, timed after the headline)")
+    ap.add_argument("--dq-in-fwd", action="store_true",
+                    help="zero the fp32 dQ accumulator with the forward's idle warps (bd_attn_fwd_ex) instead of "
+                         "in the backward's statistics kernel")
     ap.add_argument("--split", action="store_true",
                     help="needed-only windows: time window partials + the owner-sum kernel and the statistics "
                          "kernel clearing dQ, instead of the owner-row backward with dQ cleared by the forward")

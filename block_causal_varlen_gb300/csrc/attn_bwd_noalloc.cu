@@ -19,7 +19,10 @@
 //     array it reads, so nothing has to start at zero;
 //   * the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current); make that first call
-//     before any stream capture.
+//     before any stream capture. The address is kept for the life of the
+//     process, so a cudaDeviceReset (or any other teardown of the device's
+//     context) between calls is not supported: the array may then sit at a new
+//     address and the kept one would be stale.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -89,8 +89,8 @@ struct FwdCfg {
 // barrier indices (8 bytes each)
 enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14, B_SFULL = 18,
-  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_UFULL = 27, B_UEMPTY = 27 + kUnitSlots,
-  B_COUNT = 27 + 2 * kUnitSlots
+  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_TURN = 28, B_UFULL = 30,
+  B_UEMPTY = 30 + kUnitSlots, B_COUNT = 30 + 2 * kUnitSlots
 };
 static_assert(8 * B_COUNT + 16 + 4 * kUnitSlots <= 512, "barriers, TMEM slot, abort flag and unit ring overflow their region");
 
@@ -120,26 +120,28 @@ __global__ void __launch_bounds__(384, 1)
   const int slots = a.slots;
 
   if (threadIdx.x == 0) {
+    // each slot's MMA thread releases the shared Q / K / V stages: one arrival per slot
     mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QEMPTY), 1);
+    mbar_init(bar(B_QEMPTY), slots);
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_KEMPTY + s), slots);
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_VEMPTY + s), slots);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_PFULL + s), 128);
       mbar_init(bar(B_OFINAL + s), 1);
       mbar_init(bar(B_OEMPTY + s), 128);
+      mbar_init(bar(B_DRAIN + s), 1);
+      mbar_init(bar(B_TURN + s), 1);
     }
-    mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < kUnitSlots; ++s) {
       mbar_init(bar(B_UFULL + s), 1);
-      mbar_init(bar(B_UEMPTY + s), 1 + 4 * slots);  // the MMA thread and each active softmax warp
+      mbar_init(bar(B_UEMPTY + s), 5 * slots);  // each slot's MMA thread and softmax warps
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -218,28 +220,49 @@ __global__ void __launch_bounds__(384, 1)
         if (qi > 0) mbar_wait_drain(bar(B_QFULL), (qi - 1) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (warp == 2 && slots == 2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per query-head slot (warp 1: slot 0, warp 2: slot 1) issues that
+    // slot's S = Q K^T and O += P V. An MMA issue only returns once the tensor pipe
+    // has taken the previous one, so a single issuer leaves the pipe idle while it
+    // commits or checks a barrier. The two issuers take turns group by group (a
+    // group: a slot's PV then its next S), which keeps the slots' softmaxes
+    // staggered as with one issuer, while each one's commits and barrier checks
+    // overlap the other's issue. B_TURN + s completes when slot s may issue its
+    // next group.
     if (lane == 0) {
+      const int s = warp - 1;
+      const bool turns = slots == 2;
+      uint32_t my_turn = 0;  // groups this slot has issued
+      // waits for this slot's turn (slot 0 goes first) and, after the group,
+      // hands the turn to the other slot
+      auto take_turn = [&]() -> bool {
+        if (!turns || (s == 0 && my_turn == 0)) return true;
+        const uint32_t k = s == 0 ? my_turn - 1 : my_turn;  // the other slot's groups done before mine
+        return mbar_wait_spin(bar(B_TURN + s), k & 1, abort_flag);
+      };
+      auto pass_turn = [&]() {
+        if (turns) mbar_arrive(bar(B_TURN + (s ^ 1)));
+        ++my_turn;
+      };
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      const uint32_t d_s = tmem + s * 128, d_o = tmem + Cfg::kOCol + s * D;
+      const uint32_t qa = sdesc_lo(sQ + s * Cfg::kTileBytes, 16);
       // descriptors are built once per operand tile; a K step only advances the
       // start-address field (16-byte units) with a 64-bit add
-      auto issue_s = [&](int s, int st) {
-        const uint32_t d_t = tmem + s * 128;
-        const uint32_t qa = sdesc_lo(sQ + s * Cfg::kTileBytes, 16), kb = sdesc_lo(sK + st * Cfg::kTileBytes, 16);
+      auto issue_s = [&](int st) {
+        const uint32_t kb = sdesc_lo(sK + st * Cfg::kTileBytes, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = uint32_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_ss_lo(d_t, qa + off, kb + off, idS, kk > 0);
+          mma_ss_lo(d_s, qa + off, kb + off, idS, kk > 0);
         }
       };
-      auto issue_pv = [&](int s, int st, bool acc) {
-        const uint32_t d_t = tmem + Cfg::kOCol + s * D;
-        const uint32_t p_t = tmem + s * 128;
+      auto issue_pv = [&](int st, bool acc) {
         const uint32_t vb = sdesc_lo(sV + st * Cfg::kTileBytes, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts_lo(d_t, p_t + kk * 8, vb + uint32_t(kk * 128), idPV, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) mma_ts_lo(d_o, d_s + kk * 8, vb + uint32_t(kk * 128), idPV, (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t kv_it = 0, qi = 0, tcount = 0;
       bool ok = true;
@@ -253,13 +276,11 @@ __global__ void __launch_bounds__(384, 1)
         {
           const int sk0 = kv_it % NK;
           if (!(ok = mbar_wait(bar(B_KFULL + sk0), (kv_it / NK) & 1, abort_flag))) break;
+          if (!(ok = take_turn())) break;
           tc_fence_after();
-          issue_s(0, sk0);
-          tc_commit(bar(B_SFULL + 0));
-          if (slots == 2) {
-            issue_s(1, sk0);
-            tc_commit(bar(B_SFULL + 1));
-          }
+          issue_s(sk0);
+          pass_turn();
+          tc_commit(bar(B_SFULL + s));
           tc_commit(bar(B_KEMPTY + sk0));
           if (nt == 1) tc_commit(bar(B_QEMPTY));
         }
@@ -267,29 +288,25 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t itp = kv_it + j - 1, itn = kv_it + j;
           const int svp = itp % NV, skn = itn % NK;
           const uint32_t tp = tcount + j - 1;
-          if (j < nt && !(ok = mbar_wait(bar(B_KFULL + skn), (itn / NK) & 1, abort_flag))) break;
-          BD_TRACE_EVENT(18, int(tp));  // MMA: next K tile present
+          BD_TRACE_EVENT(14 + s, int(tp));  // MMA: starts waiting for P
+          if (!(ok = mbar_wait_spin(bar(B_PFULL + s), tp & 1, abort_flag))) break;
+          if (j == 1 && !(ok = mbar_wait(bar(B_OEMPTY + s), (qi & 1) ^ 1, abort_flag))) break;
           if (!(ok = mbar_wait(bar(B_VFULL + svp), (itp / NV) & 1, abort_flag))) break;
-          BD_TRACE_EVENT(19, int(tp));  // MMA: V tile present
-          for (int s = 0; s < slots; ++s) {
-            BD_TRACE_EVENT(14 + s, int(tp));  // MMA: starts waiting for P
-            if (!(ok = mbar_wait(bar(B_PFULL + s), tp & 1, abort_flag))) break;
-            if (j == 1 && !(ok = mbar_wait(bar(B_OEMPTY + s), (qi & 1) ^ 1, abort_flag))) break;
-            tc_fence_after();
-            BD_TRACE_EVENT(10 + s, int(tp));  // MMA: P ready, PV issued
-            issue_pv(s, svp, j > 1);
-            if (s == slots - 1) tc_commit(bar(B_VEMPTY + svp));
-            if (j < nt) {
-              issue_s(s, skn);
-              BD_TRACE_EVENT(12 + s, int(tcount + j));  // MMA: S issued
-              tc_commit(bar(B_SFULL + s));
-              if (s == slots - 1) {
-                tc_commit(bar(B_KEMPTY + skn));
-                if (j == nt - 1) tc_commit(bar(B_QEMPTY));
-              }
-            } else {
-              tc_commit(bar(B_OFINAL + s));
-            }
+          if (j < nt && !(ok = mbar_wait(bar(B_KFULL + skn), (itn / NK) & 1, abort_flag))) break;
+          if (!(ok = take_turn())) break;
+          tc_fence_after();
+          BD_TRACE_EVENT(10 + s, int(tp));  // MMA: P ready, PV issued
+          issue_pv(svp, j > 1);
+          if (j < nt) issue_s(skn);
+          pass_turn();
+          tc_commit(bar(B_VEMPTY + svp));
+          if (j < nt) {
+            BD_TRACE_EVENT(12 + s, int(tcount + j));  // MMA: S issued
+            tc_commit(bar(B_SFULL + s));
+            tc_commit(bar(B_KEMPTY + skn));
+            if (j == nt - 1) tc_commit(bar(B_QEMPTY));
+          } else {
+            tc_commit(bar(B_OFINAL + s));
           }
         }
         kv_it += nt;
@@ -297,17 +314,17 @@ __global__ void __launch_bounds__(384, 1)
         ++qi;
       }
       if (!ok) {
-        tc_commit(bar(B_DRAIN));
-        mbar_wait_drain(bar(B_DRAIN), 0);
+        tc_commit(bar(B_DRAIN + s));
+        mbar_wait_drain(bar(B_DRAIN + s), 0);
       }
     }
    }
-   else {
-    // warps 2-3: zero the caller's dQ accumulator (one d-vector of one (row, head)
+   else if (warp == 3) {
+    // warp 3: zero the caller's dQ accumulator (one d-vector of one (row, head)
     // per warp store round), spread over every CTA of the launch
     if (a.dqz != nullptr) {
       const int64_t nvec = int64_t(a.B) * a.C * a.L * a.H;
-      for (int64_t vid = int64_t(blockIdx.x) * 2 + (warp - 2); vid < nvec; vid += int64_t(gridDim.x) * 2) {
+      for (int64_t vid = blockIdx.x; vid < nvec; vid += gridDim.x) {
         const int h = int(vid % a.H);
         const int64_t r = vid / a.H;
         const int l = int(r % a.L);
@@ -320,17 +337,15 @@ __global__ void __launch_bounds__(384, 1)
     }
 #ifdef BD_TRACE
     if (lane == 0 && blockIdx.x == 0) {
-      // tracing build only: stamp the moment each K (warp 2) / V (warp 3) tile lands
-      const bool isk = warp == 2;
-      const int n = isk ? NK : NV;
+      // tracing build only: stamp the moment each K tile lands
       for (uint32_t it = 0; it < uint32_t(kTraceTiles); ++it) {
-        const uint32_t fb = bar((isk ? B_KFULL : B_VFULL) + int(it % n)), par = (it / n) & 1;
+        const uint32_t fb = bar(B_KFULL + int(it % NK)), par = (it / NK) & 1;
         const uint64_t t0 = globaltimer();
         bool got = false;
         while (!(got = mbar_try_wait(fb, par)) && globaltimer() - t0 < 20000000ull) {
         }
         if (!got) break;
-        BD_TRACE_EVENT(isk ? 26 : 27, int(it));
+        BD_TRACE_EVENT(26, int(it));
       }
     }
 #endif

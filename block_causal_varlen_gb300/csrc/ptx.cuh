@@ -80,6 +80,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that polls without the suspend hint: for the MMA-issuing threads,
+// whose waits sit on the tensor pipe's critical path (a parked thread resumes
+// later than a polling one). Checks the abort flag and the time limit every 64
+// polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait used while shutting down after a failure: ignores the abort
 // flag so that copies and MMAs already in flight are still waited for.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {

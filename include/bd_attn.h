@@ -341,7 +341,9 @@ BD_API int32_t bd_owner_sum_ex(const void* plan_host, const void* plan_dev, cons
  * bd_attn_bwd_noalloc_capacity() return BD_ERR_CAPACITY before any launch.
  * All calls on a device share the array: calls that may overlap on the GPU
  * race and must be ordered by the caller. The first call on a device looks up
- * the array's address; make it before any stream capture. Arguments and
+ * the array's address; make it before any stream capture. That address is kept
+ * until the process exits: resetting the device (cudaDeviceReset) between calls
+ * is not supported. Arguments and
  * results are those of bd_attn_bwd without the workspace. */
 BD_API int32_t bd_attn_bwd_noalloc(const void* plan_host, const void* plan_dev, const bd_tensor* q,
                             const bd_tensor* k, const bd_tensor* v, const bd_tensor* out,

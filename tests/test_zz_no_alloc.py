@@ -5,14 +5,19 @@ library instead of a caller buffer.
 
 Called through the C ABI (ctypes), it must give the same gradients as
 bd_attn_bwd with a caller workspace, on two calls in a row (the shared array
-keeps the previous call's contents), and must refuse plans whose workspace
-does not fit the array before launching anything. This file is collected
-last; it passes alone in a fresh process and after the other tests."""
+keeps the previous call's contents): dK / dV bit for bit (they accumulate in
+a fixed order), dQ up to the order of its fp32 reduce-adds, also when adding
+into existing dK / dV and at head dim 256 (its own kernel); and it must refuse
+plans whose workspace does not fit the array before launching anything. This
+file is collected last; it passes alone in a fresh process and after the other
+tests."""
 import ctypes as C
+import dataclasses
 
 import pytest
 import torch
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -28,45 +33,51 @@ def _gpu():
     bd.load()
 
 
-def _call_noalloc(lib, plan, qd, kd, vd, out, dod, lse, dq, dk, dv):
+def _call_noalloc(lib, plan, qd, kd, vd, out, dod, lse, dq, dk, dv, accumulate=0):
     ts = [bd._tensor(x, n) for x, n in ((qd, "q"), (kd, "k"), (vd, "v"), (out, "out"), (dod, "dout"))]
     tl = bd._rowstat(lse, "lse")
     tq, tk, tv = bd._tensor(dq, "dq"), bd._tensor(dk, "dk"), bd._tensor(dv, "dv")
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.bd_attn_bwd_noalloc(plan.host_ptr, plan.dev_ptr, *[C.byref(t) for t in ts], C.byref(tl),
-                                   C.byref(tq), C.byref(tk), C.byref(tv), 0, stream)
+                                   C.byref(tq), C.byref(tk), C.byref(tv), accumulate, stream)
 
 
-@pytest.mark.parametrize("i,mode", [(2, bd.BD_KV_GATHER), (3, bd.BD_KV_WINDOW)])
-def test_noalloc_matches_workspace_backward_twice(i, mode):
+@pytest.mark.parametrize("i,mode,d,acc", [(2, bd.BD_KV_GATHER, 128, 0), (3, bd.BD_KV_WINDOW, 128, 0),
+                                          (1, bd.BD_KV_GATHER, 256, 1), (2, bd.BD_KV_WINDOW, 256, 1)])
+def test_noalloc_matches_workspace_backward_twice(i, mode, d, acc):
     lib = bd.load()
-    wl = workloads.config(i)
+    wl = dataclasses.replace(workloads.config(i), d=d)
     q, k, v, do = workloads.tensors(wl)
     plan, out, lse, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, mode)
     assert bd.bd_attn_bwd_workspace(plan) <= lib.bd_attn_bwd_noalloc_capacity()
     dod = gu.as_chunks(do.cuda(), wl.cp)
-    ref = [torch.empty(qd.shape, dtype=torch.float32, device="cuda"),
-           torch.empty(kd.shape, dtype=torch.float32, device="cuda"),
-           torch.empty(vd.shape, dtype=torch.float32, device="cuda")]
+    g = torch.Generator().manual_seed(11)
+    # dK / dV start from random values when adding into them, from zeros otherwise
+    # (window rows past each chunk's window are not written)
+    dk0 = torch.randn(kd.shape, generator=g).cuda() if acc else torch.zeros(kd.shape, device="cuda")
+    dv0 = torch.randn(vd.shape, generator=g).cuda() if acc else torch.zeros(vd.shape, device="cuda")
+    ref = [torch.empty(qd.shape, dtype=torch.float32, device="cuda"), dk0.clone(), dv0.clone()]
     ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
-    bd.bd_attn_bwd(plan, qd, kd, vd, out, dod, lse, *ref, ws)
+    bd.bd_attn_bwd(plan, qd, kd, vd, out, dod, lse, *ref, ws, accumulate_dkv=bool(acc))
     torch.cuda.synchronize()
     for call in range(2):
-        got = [torch.full_like(t, float("nan")) for t in ref]
-        st = _call_noalloc(lib, plan, qd, kd, vd, out, dod, lse, *got)
+        got = [torch.full_like(ref[0], float("nan")), dk0.clone(), dv0.clone()]
+        st = _call_noalloc(lib, plan, qd, kd, vd, out, dod, lse, *got, accumulate=acc)
         assert st == 0, lib.bd_last_error().decode()
         torch.cuda.synchronize()
         bd.bd_check_status(plan)
-        for g, r, name in zip(got, ref, ("dQ", "dK", "dV")):
-            if mode == bd.BD_KV_WINDOW and name != "dQ":
-                # rows past each chunk's window are not part of the result
-                for c in range(wl.cp):
-                    hdr, _ = plan.chunk(c)
-                    n = hdr["kv_end"] - hdr["kv_start"]
-                    g[:, c, n:] = 0
-                    r[:, c, n:] = 0
-            assert torch.isfinite(g).all(), f"call {call}: {name} not fully written"
-            assert gu.max_rel(g.cpu(), r.cpu()) <= gu.GRAD_REL, f"call {call}: {name}"
+        assert torch.isfinite(got[0]).all(), f"call {call}: dQ not fully written"
+        assert gu.max_rel(got[0].cpu(), ref[0].cpu()) <= 1e-5, f"call {call}: dQ"
+        assert torch.equal(got[1], ref[1]), f"call {call}: dK differs from the workspace form"
+        assert torch.equal(got[2], ref[2]), f"call {call}: dV differs from the workspace form"
+    if i == 1:   # and against the oracle, sequence 0, all-gathered K/V
+        gq, gk, gv, _, _ = oracle.attention_bwd(q[0], k[0], v[0], do[0], wl.cu[0])
+        dq_, dk_, dv_ = (t.view(wl.S, -1, wl.d).cpu() for t in got)
+        base_k = dk0.view(wl.S, -1, wl.d).cpu() if acc else 0
+        base_v = dv0.view(wl.S, -1, wl.d).cpu() if acc else 0
+        assert gu.max_rel(dq_, gq) <= gu.GRAD_REL
+        assert gu.max_rel(dk_ - base_k, gk) <= gu.GRAD_REL
+        assert gu.max_rel(dv_ - base_v, gv) <= gu.GRAD_REL
 
 
 def test_noalloc_rejects_plans_beyond_its_capacity():
