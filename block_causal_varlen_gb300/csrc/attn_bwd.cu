@@ -54,11 +54,18 @@ struct BwdCfg {
   static constexpr int kOffQ = 2 * kTileBytes;          // two stages
   static constexpr int kOffDO = 4 * kTileBytes;
   static constexpr int kOffDS = 5 * kTileBytes;         // dS^T, 128 keys x 128 queries bf16
-  static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128], ds[128]
-  static constexpr int kStatBytes = 3 * 512;
-  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;  // dQ staging, two 128 rows x 64 bytes buffers
-  static constexpr int kOffBar = kOffStage + 16384;
-  static constexpr int kSmem = kOffBar + 256 + 1024;
+  static constexpr int kOffStat = kOffDS + 32768;       // per stage: lse2[128], D[128]
+  static constexpr int kStatBytes = 2 * 512;
+  // dQ staging: two buffers of one 128 rows x 32 columns fp32 reduce box (16 KB,
+  // 128-byte swizzle): a TMA reduce-add costs ~425 cycles per box up to 8 KB and
+  // ~712 for 16 KB, so 16 KB boxes move dQ ~20% faster than 8 KB ones
+  static constexpr int kOffStage = kOffStat + 2 * kStatBytes;
+  static constexpr int kStageBytes = 128 * 32 * 4;
+  static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
+  // no alignment slack: the dynamic shared memory base must be 1024-byte aligned
+  // (checked at kernel entry; the kernel records a failure and does nothing if not)
+  static constexpr int kSmem = kOffBar + 256;
+  static_assert(kSmem <= 232448, "shared memory over the per-CTA limit");
   static constexpr int kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kThreads = 512;
   // register split after setmaxnreg: producer/MMA, P/dS warpgroups, dQ warpgroup
@@ -83,9 +90,18 @@ __global__ void __launch_bounds__(512, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using Cfg = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
+  // the 128-byte-swizzled operand tiles need 1024-byte alignment and the layout
+  // leaves no slack to round up: refuse (and record why) rather than overrun
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) {
+      atomicExch(const_cast<int32_t*>(a.plan) + H_STATUS, DEV_SMEM_ALIGN);
+      atomicExch(const_cast<int32_t*>(a.plan) + H_STATUS_DETAIL, 2);
+    }
+    return;
+  }
   const uint32_t sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV, sQ = sbase + Cfg::kOffQ;
   const uint32_t sDO = sbase + Cfg::kOffDO, sDS = sbase + Cfg::kOffDS, sStage = sbase + Cfg::kOffStage;
   const uint32_t bars = sbase + Cfg::kOffBar;
@@ -165,7 +181,6 @@ __global__ void __launch_bounds__(512, 1)
           const int64_t srow = (int64_t(x.it) * a.H + x.h) * a.Lpad + x.t * 128;
           bulk_load(st, a.lse2 + srow, 512, bar(C_QFULL0 + qs));
           bulk_load(st + 512, a.dstat + srow, 512, bar(C_QFULL0 + qs));
-          bulk_load(st + 1024, a.rowds + int64_t(x.it) * a.Lpad + x.t * 128, 512, bar(C_QFULL0 + qs));
           ++q_iss;
           if (!(ok = mbar_wait(bar(C_DOEMPTY), (sc & 1) ^ 1, abort_flag))) return;
           mbar_expect_tx(bar(C_DOFULL), Cfg::kTileBytes);
@@ -318,7 +333,13 @@ __global__ void __launch_bounds__(512, 1)
             const int i0 = r0 + t * 128;  // global row of query column 0
             const float* st_lse = reinterpret_cast<const float*>(smem + Cfg::kOffStat + qs * Cfg::kStatBytes);
             const float* st_d = st_lse + 128;
-            const int32_t* st_ds = reinterpret_cast<const int32_t*>(st_lse + 256);
+            // the query rows' document starts come from global memory (the workspace),
+            // read before the waits so that their latency hides behind them: the last
+            // row's for the whole-tile test, and lane l's row of each 32-column chunk
+            // for masking (shared with the other lanes by shuffles)
+            const int32_t* g_ds = a.rowds + int64_t(it) * a.Lpad + t * 128;
+            const int ds_last = __ldg(g_ds + 127);
+            const int ds_mine0 = __ldg(g_ds + half * 64 + lane), ds_mine1 = __ldg(g_ds + half * 64 + 32 + lane);
             if (!(ok = mbar_wait(bar(C_QFULL0 + qs), (sc >> 1) & 1, abort_flag))) break;
             if (threadIdx.x == 128) BD_TRACE_EVENT(10, int(sc));  // compute: waits S
             if (!(ok = mbar_wait(bar(C_SFULL), sc & 1, abort_flag))) break;
@@ -327,7 +348,7 @@ __global__ void __launch_bounds__(512, 1)
             // Rows' document starts are non-decreasing and invalid rows carry
             // INT_MAX, so key j sees every query of the tile iff it lies at or
             // before the tile's first row and at or after the last row's doc start.
-            const bool full = (j <= i0) && (j >= st_ds[127]);
+            const bool full = (j <= i0) && (j >= ds_last);
             // P^T is kept as the bf16 pairs written to TMEM (the dV MMA reads the same
             // rounded values); dS below unpacks them
             uint32_t pk[2][16];
@@ -348,11 +369,15 @@ __global__ void __launch_bounds__(512, 1)
                 for (int k = 0; k < 4; ++k)
                   p[4 * e4 + k] = ex2(fmaf(__uint_as_float(r[4 * e4 + k]), a.scale_log2, -lv[k]));
               }
-              if (!full) {
+              // (lanes are keys, so the whole-tile test differs across the warp: every
+              // lane takes part in the shuffles whenever one of them masks)
+              if (__any_sync(0xffffffffu, !full)) {
+                const int ds_mine = ch ? ds_mine1 : ds_mine0;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                   const int i = ib + e;
-                  if (!((j >= st_ds[i]) && (j <= i0 + i))) p[e] = 0.f;
+                  const int ds_i = __shfl_sync(0xffffffffu, ds_mine, e);
+                  if (!full && !((j >= ds_i) && (j <= i0 + i))) p[e] = 0.f;
                 }
               }
 #pragma unroll
@@ -515,18 +540,18 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(bar(C_DQEMPTY));
             if (rl == 0) BD_TRACE_EVENT(22, int(sc));  // dQ: TMEM released
-            // D/16 rounds of 128 rows x 16 columns through two 8 KB staging buffers
-            // (64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)), so
-            // that filling one buffer overlaps the TMA reading the other
+            // D/32 rounds of 128 rows x 32 columns (16 KB) through two staging buffers
+            // (128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7)), so that
+            // filling one buffer overlaps the TMA reading the other
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q) {
-              const uint32_t buf = sStage + (q & 1) * 8192;
+            for (int q = 0; q < D / 32; ++q) {
+              const uint32_t buf = sStage + (q & 1) * Cfg::kStageBytes;
               if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
               named_bar_sync(1, 128);
-              const uint32_t* v = r[q >> 1] + (q & 1) * 16;
+              const uint32_t* v = r[q];
 #pragma unroll
-              for (int c4 = 0; c4 < 4; ++c4)
-                st_shared_v4(buf + rl * 64 + ((c4 ^ ((rl >> 1) & 3)) << 4),
+              for (int c4 = 0; c4 < 8; ++c4)
+                st_shared_v4(buf + rl * 128 + ((c4 ^ (rl & 7)) << 4),
                              __float_as_uint(__uint_as_float(v[4 * c4]) * a.scale),
                              __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * a.scale),
                              __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * a.scale),
@@ -534,7 +559,7 @@ __global__ void __launch_bounds__(512, 1)
               fence_proxy_async_smem();
               named_bar_sync(1, 128);
               if (rl == 0) {
-                tma_reduce_add_5d(&tm_dq, buf, q * 16, h, t * 128, c, b);
+                tma_reduce_add_5d(&tm_dq, buf, q * 32, h, t * 128, c, b);
                 bulk_commit();
               }
             }
@@ -748,11 +773,11 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
     return fail(BD_ERR_ARG, "dk/dv rows < %d", pv.hdr(H_KV_ROWS));
   }
   CUtensorMap mq, mk, mv, mdo, mdq;
-  // dQ reduce boxes: 128 rows x 16 columns (64-byte swizzle), or at head dim 256
-  // (transposed dQ) 16 rows x 32 columns (128-byte swizzle); Q / dO boxes are one
-  // backward query step high
+  // dQ reduce boxes: 128 rows x 32 columns (128-byte swizzle), or at head dim 256
+  // (transposed dQ) 16 rows x 32 columns; Q / dO boxes are one backward query
+  // step high
   if ((st = c.D == 256 ? make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 16)
-                       : make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq")))
+                       : make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 128)))
     return st;
   if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q", bwd_query_step(c.D)))) return st;
   if ((st = make_tmap_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout", bwd_query_step(c.D)))) return st;

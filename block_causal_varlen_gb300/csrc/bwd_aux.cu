@@ -230,5 +230,9 @@ extern "C" int32_t bd_check_status(const void* plan_dev, int32_t reset, void* st
   }
   if (host[0] == DEV_TIMEOUT)
     return fail(BD_ERR_DEVICE_TIMEOUT, "a kernel stopped after a bounded wait timed out (site %d)", host[1]);
+  if (host[0] == DEV_SMEM_ALIGN)
+    return fail(BD_ERR_CUDA, "a kernel found its shared memory not 1024-byte aligned and did no work (site %d)",
+                host[1]);
+  if (host[0] != DEV_OK) return fail(BD_ERR_CUDA, "a kernel recorded failure code %d (site %d)", host[0], host[1]);
   return ok();
 }

@@ -76,6 +76,6 @@ enum : int {
 constexpr int bwd_query_step(int d) { return d == 256 ? 64 : kTile; }
 
 // device failure codes stored at H_STATUS
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_SMEM_ALIGN = 2 };
 
 }  // namespace bd

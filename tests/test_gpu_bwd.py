@@ -69,6 +69,9 @@ def test_bwd_full_elementwise(i, mode):
         grad_check(dq[b], gq, "dQ")
         grad_check(dk[b], gk, "dK")
         grad_check(dv[b], gv, "dV")
+        # per document too: a wrong short document would hide under the tensor maximum
+        for got, want, name in ((dq[b], gq, "dQ"), (dk[b], gk, "dK"), (dv[b], gv, "dV")):
+            assert gu.doc_rel(got, want, wl.cu[b]) <= gu.GRAD_REL, f"{name}: per-document max-rel"
         pad = wl.cu[b][-1]
         assert not dq[b, pad:].any() and not dk[b, pad:].any() and not dv[b, pad:].any()
 

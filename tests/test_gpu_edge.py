@@ -72,9 +72,14 @@ def test_edge_layout_fwd_bwd(name, mode, d):
             assert gu.max_rel(dk[0, r, :e - a], dkw) <= gu.GRAD_REL
             assert gu.max_rel(dv[0, r, :e - a], dvw) <= gu.GRAD_REL
     if mode == bd.BD_KV_GATHER:
-        _, dk_ref, dv_ref, _, _ = oracle.attention_bwd(q[0], k[0], v[0], do[0], cu)
+        dq_ref, dk_ref, dv_ref, o_ref, _ = oracle.attention_bwd(q[0], k[0], v[0], do[0], cu)
         assert gu.max_rel(dk[0, 0], dk_ref) <= gu.GRAD_REL
         assert gu.max_rel(dv[0, 0], dv_ref) <= gu.GRAD_REL
+        # per document too: a wrong short document would hide under the tensor maximum
+        assert gu.doc_rel(dq.view(wl.S, wl.H, wl.d), dq_ref, cu) <= gu.GRAD_REL
+        assert gu.doc_rel(dk[0, 0], dk_ref, cu) <= gu.GRAD_REL
+        assert gu.doc_rel(dv[0, 0], dv_ref, cu) <= gu.GRAD_REL
+        assert gu.doc_rel(out[0].reshape(wl.S, wl.H, wl.d).float(), o_ref, cu) <= gu.O_REL
         # padding rows and columns: exact zeros
         sv = cu[-1]
         assert not dq.view(wl.S, wl.H, wl.d)[sv:].abs().sum().item()

@@ -36,6 +36,10 @@ def test_fwd_full_elementwise(i, mode):
             o_ref, l_ref = oracle.chunk_fwd(q[b, rows], k[b], v[b], wl.cu[b], wl.S, r * wl.L)
             gu.o_check(out[b, r].float(), o_ref)
             gu.lse_check(lse[b, r], l_ref)
+        # per document too, over the whole sequence (a wrong short document would hide
+        # under the tensor maximum)
+        o_full, _ = oracle.attention_fwd(q[b], k[b], v[b], wl.cu[b], dtype=torch.float32 if i > 1 else torch.float64)
+        assert gu.doc_rel(out[b].reshape(wl.S, wl.H, wl.d).float(), o_full, wl.cu[b]) <= gu.O_REL
 
 
 @pytest.mark.parametrize("mode", MODES)
