@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * E_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 8 * E_COUNT + 8);
   volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + C::kOffBar + 8 * E_COUNT + 16);
-  int* claim = const_cast<int32_t*>(a.plan) + H_BWD_CLAIM;
+  int* claim = a.counters;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(512, 1)
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 2);
     }
-    unit_counters_release(claim, const_cast<int32_t*>(plan) + H_BWD_DONE);
+    unit_counters_release(claim, claim + 1);
   }
 }
 

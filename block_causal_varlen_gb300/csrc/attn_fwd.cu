@@ -32,6 +32,7 @@
 
 #include <math_constants.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "host_util.h"
@@ -57,6 +58,7 @@ struct FwdArgs {
   float* dqz;
   int64_t z_sb, z_sc, z_sr, z_sh;
   int32_t B, C, H;
+  int32_t counter_slot;  // which (claim, done) pair of the plan's forward counter slots
 };
 
 template <int D>
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * B_COUNT + 8);
   volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT + 16);
-  int* claim = const_cast<int32_t*>(a.plan) + H_FWD_CLAIM;
+  int* claim = const_cast<int32_t*>(a.plan) + H_FWD_SLOTS + 2 * a.counter_slot;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(384, 1)
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 1);
     }
-    unit_counters_release(claim, const_cast<int32_t*>(plan) + H_FWD_DONE);
+    unit_counters_release(claim, claim + 1);
   }
 }
 
@@ -638,6 +640,11 @@ extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, c
   a.z_sb = dq_zero ? dq_zero->stride_b : 0; a.z_sc = dq_zero ? dq_zero->stride_c : 0;
   a.z_sr = dq_zero ? dq_zero->stride_row : 0; a.z_sh = dq_zero ? dq_zero->stride_head : 0;
   a.B = B; a.C = C; a.H = H;
+  // each launch takes the next counter slot: launches sharing the device plan may
+  // then overlap on the GPU (up to kFwdCounterSlots at once) without taking each
+  // other's work units
+  static std::atomic<uint32_t> launch_seq{0};
+  a.counter_slot = int32_t(launch_seq.fetch_add(1, std::memory_order_relaxed) % kFwdCounterSlots);
   float scale;
   const int32_t scale_bits = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &scale_bits, 4);

@@ -26,7 +26,10 @@ BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
   w.lse2 = 0;
   w.dstat = stat;
   w.rowds = 2 * stat;
-  w.total = 2 * stat + al(size_t(nitems) * Lpad * sizeof(int32_t));
+  // the main kernel's work-unit claim counters live in the caller's workspace, so
+  // backward launches that share a device plan but not a workspace may overlap
+  w.counters = 2 * stat + al(size_t(nitems) * Lpad * sizeof(int32_t));
+  w.total = w.counters + 256;
   return w;
 }
 
@@ -40,6 +43,7 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   const int item = blockIdx.x / a.Lpad, l = blockIdx.x % a.Lpad;
   const int b = item / a.C, c = item % a.C;
   const int tid = threadIdx.x;
+  if (blockIdx.x == 0 && tid < 2) a.counters[tid] = 0;  // the main kernel's claim counters
   constexpr int CPH = D / 8;  // 16-byte pieces per head (8, 16 or 32: groups never straddle a warp)
   const float inf = __int_as_float(0x7f800000);
   if (l >= a.L) {

@@ -17,6 +17,7 @@ struct BwdPreArgs {
   float* lse2;     // workspace [nitems, H, Lpad]: LSE * log2(e), +inf on invalid rows
   float* dstat;    // workspace [nitems, H, Lpad]: D = <dO, O>
   int32_t* rowds;  // workspace [nitems, Lpad]: global start row of the row's document, INT_MAX if invalid
+  int32_t* counters;  // workspace: the main kernel's (claim, done) work-unit counters, zeroed here
   float* dq;       // zeroed when clear_dq is set
   int64_t q_sb, q_sc, q_sr, q_sh;
   int32_t nitems, C, L, Lpad, H, clear_dq;
@@ -24,7 +25,7 @@ struct BwdPreArgs {
 
 // Workspace layout of the backward (offsets in bytes, 256-byte aligned).
 struct BwdWorkspace {
-  size_t lse2, dstat, rowds, total;
+  size_t lse2, dstat, rowds, counters, total;
 };
 BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad);
 

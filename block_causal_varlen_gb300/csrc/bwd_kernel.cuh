@@ -15,6 +15,7 @@ struct BwdArgs {
   const float* lse2;
   const float* dstat;
   const int32_t* rowds;
+  int32_t* counters;  // (claim, done) work-unit counters in the workspace
   float* dq;
   int64_t q_sb, q_sc, q_sr, q_sh;
   float* dk;

@@ -24,12 +24,10 @@ enum : int {
   H_DROP_SEED_HI,
   H_OFF_BWDO,           // backward work units keyed by owner rows (BD_KV_WINDOW plans
   H_NBWDO,              // of every chunk in order with L % 128 == 0; else 0 units)
+  H_FWD_SLOTS = 38,     // kFwdCounterSlots (claim, done) pairs of forward work-unit
+                        // counters, one pair per launch in flight (0 between launches)
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
   H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
-  H_FWD_CLAIM = 58,     // forward work-unit claim counter (0 between launches)
-  H_FWD_DONE = 59,      // forward CTAs finished in the current launch
-  H_BWD_CLAIM = 60,     // the same two counters for the backward main kernel
-  H_BWD_DONE = 61,
   kHdrWords = 64
 };
 
@@ -77,5 +75,11 @@ constexpr int bwd_query_step(int d) { return d == 256 ? 64 : kTile; }
 
 // device failure codes stored at H_STATUS
 enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_SMEM_ALIGN = 2 };
+
+// Forward launches take their work-unit counters from one of these slots in the
+// device plan, in turn (launch k uses slot k mod kFwdCounterSlots), so that up to
+// this many forward launches sharing one device plan may run at the same time.
+constexpr int kFwdCounterSlots = 8;
+static_assert(H_FWD_SLOTS + 2 * kFwdCounterSlots <= H_STATUS, "forward counter slots overlap the status words");
 
 }  // namespace bd

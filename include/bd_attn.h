@@ -91,7 +91,13 @@ typedef struct {
   int32_t S, cp, rank, L, row_offset, s_valid, n_pad, kv_start, kv_end, nseg;
 } bd_chunk_hdr;
 
-/* bd_segment -- varlen metadata of chunk `rank` of `cp` for one packed sequence.
+/* bd_segment -- varlen metadata of chunk `rank` of `cp` for one packed sequence:
+ * the contiguous rows [rank*L, (rank+1)*L) (NeMo Automodel page "block-diagonal
+ * varlen CP for packed sequences", Design overview, batch.py), cut into one
+ * segment per document they overlap (Design overview, kernels.py), a document
+ * straddling the left edge giving more keys than queries with bottom-right
+ * alignment (Key correctness property 2), every index validated here on the
+ * host (Key correctness property 4).
  *   cu_seqlens  host int32[ndocs+1], cu_seqlens[0] = 0, non-decreasing,
  *               cu_seqlens[ndocs] <= S. Zero-length documents are allowed and
  *               produce no segment.
@@ -166,13 +172,18 @@ BD_API int32_t bd_plan_bytes(const bd_plan_desc* desc, size_t* bytes);
 
 /* Build the plan blob into caller-owned host memory `blob` (16-byte aligned,
  * blob_bytes >= bd_plan_bytes). The caller copies the same bytes once per step
- * to device memory (16-byte aligned, writable: kernels record a failure
- * status in it, and the forward and backward-main kernels keep their work-unit
- * claim counters in it, which the last CTA of each launch returns to zero) and
- * passes both copies to the attention calls, which size their launches from
- * the host copy and read the device copy. Launches of the same kernel that
- * share one device copy must therefore be ordered (one stream, or events):
- * two of them running at once would take units from each other. */
+ * to device memory (16-byte aligned, writable: kernels record a failure status
+ * in it, and forward launches take their work-unit claim counters from 8 slots
+ * in it, launch after launch in turn, each slot returned to zero by the last CTA
+ * of its launch) and passes both copies to the attention calls, which size their
+ * launches from the host copy and read the device copy. Up to 8 forward launches
+ * sharing one device copy may run at the same time (on unordered streams); a
+ * ninth in flight would share a slot with the first and take units from it.
+ * Backward launches keep their counters in their workspace: ones that share the
+ * device plan but not the workspace may overlap. (The plan blob also holds the
+ * backward's work lists; the pages' kernels.py builds the equivalent varlen
+ * metadata once per step, NeMo Automodel page "block-diagonal varlen CP for
+ * packed sequences", Design overview.) */
 BD_API int32_t bd_plan_build(const bd_plan_desc* desc, void* blob, size_t blob_bytes);
 
 /* Read back the header of chunk item `item` (item = b*nchunks + c) and its
@@ -220,7 +231,11 @@ typedef struct {
 
 /* bd_attn_fwd -- forward of every chunk item in the plan: for each query row
  * of each chunk, O = softmax(scale * q K^T restricted to the row's document and
- * causal past) V and LSE. q, k, v bf16; out bf16 (same layout rules as q);
+ * causal past) V and LSE -- the block-causal varlen attention of a chunk's query
+ * rows against all-gathered or needed-only K/V (NeMo Automodel page
+ * "block-diagonal varlen CP for packed sequences", Summary; Key correctness
+ * properties 1 and 2), whose concatenation over chunks equals full attention
+ * under the block-causal mask. q, k, v bf16; out bf16 (same layout rules as q);
  * lse fp32. row_offset: -1 to take every chunk's offset from the plan, or
  * the expected rank*L of a single-chunk plan (checked; BD_ERR_PLAN if it
  * differs). Rows of K/V at or past s_valid must hold finite values (they are
@@ -241,11 +256,17 @@ BD_API int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, const
                        const bd_tensor* k, const bd_tensor* v, int32_t row_offset,
                        bd_tensor* out, bd_rowstat* lse, bd_tensor* dq_zero, void* stream);
 
-/* Workspace bytes bd_attn_bwd needs for this plan (softmax statistics D). */
+/* Workspace bytes bd_attn_bwd needs for this plan: per row and head D = <dO, O>
+ * and the LSE in log2 units, each row's document start, and the main kernel's
+ * work-unit counters (zeroed by bd_attn_bwd_pre). Calls that overlap on the GPU
+ * need workspaces of their own. */
 BD_API int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes);
 
 /* bd_attn_bwd -- backward of every chunk item in the plan for the loss
- * sum(out * dout). dq fp32 [B, nchunks, L, H, d] is overwritten. dk, dv fp32
+ * sum(out * dout): the analytic gradient of bd_attn_fwd, with the all-gather's
+ * backward a reduce-scatter SUM of the dK/dV partials at their owners (NeMo
+ * Automodel page "block-diagonal varlen CP for packed sequences", Design
+ * overview, exchange.py). dq fp32 [B, nchunks, L, H, d] is overwritten. dk, dv fp32
  * key-like tensors receive each K/V buffer's gradient: in BD_KV_GATHER mode
  * the contributions of all the plan's chunks of a sequence are summed into
  * that sequence's buffer (the reduce-scatter SUM done in place); in

@@ -202,20 +202,23 @@ def test_bwd_dkv_deterministic():
 
 
 def test_claim_counters_reset_between_launches():
-    """The forward and backward-main kernels take work units from claim counters
-    in the device plan; the last CTA of each launch returns them to zero, so the
-    same uploaded plan serves launch after launch with identical results."""
+    """The forward takes its work units from counter slots in the device plan (one
+    slot per launch, in turn) and the backward main kernel from counters in its
+    workspace; the last CTA of each launch returns them to zero, so the same
+    uploaded plan and workspace serve launch after launch with identical results."""
     wl = workloads.config(2)
     q, k, v, do = workloads.tensors(wl)
     mode = bd.BD_KV_WINDOW
     plan, out1, lse1, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, mode)
-    ctr = slice(58, 62)  # forward claim/done, backward claim/done
-    assert torch.count_nonzero(plan.dev[ctr]).item() == 0
+    slots = slice(38, 38 + 2 * 8)  # the forward's (claim, done) slots
+    assert torch.count_nonzero(plan.dev[slots]).item() == 0
     out2 = torch.empty_like(out1)
     lse2 = torch.empty_like(lse1)
-    bd.bd_attn_fwd(plan, qd, kd, vd, out2, lse2)
+    for _ in range(9):   # every slot used at least once
+        bd.bd_attn_fwd(plan, qd, kd, vd, out2, lse2)
     dod = gu.as_chunks(do.cuda(), wl.cp)
-    ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
+    nws = bd.bd_attn_bwd_workspace(plan)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     grads = []
     for _ in range(2):
         dq = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
@@ -225,11 +228,44 @@ def test_claim_counters_reset_between_launches():
         grads.append((dq, dk, dv))
     torch.cuda.synchronize()
     bd.bd_check_status(plan)
-    assert torch.count_nonzero(plan.dev[ctr]).item() == 0
+    assert torch.count_nonzero(plan.dev[slots]).item() == 0
+    ctr = ws[nws - 256:nws - 248].view(torch.int32)   # the backward's (claim, done)
+    assert torch.count_nonzero(ctr).item() == 0
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
     (dq1, dk1, dv1), (dq2, dk2, dv2) = grads
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # dK/dV accumulate in TMEM: deterministic
     assert gu.max_rel(dq2, dq1) < 1e-5                        # dQ adds in arrival order
+
+
+def test_overlapping_launches_on_one_plan():
+    """Forward launches that share one device plan and run at the same time on
+    unordered streams each take a counter slot of their own and give the outputs
+    of a lone launch; so do backward launches sharing the plan but with a
+    workspace each."""
+    wl = workloads.config(2)
+    q, k, v, do = workloads.tensors(wl)
+    plan, out_ref, lse_ref, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, bd.BD_KV_GATHER)
+    dod = gu.as_chunks(do.cuda(), wl.cp)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = [(torch.empty_like(out_ref), torch.empty_like(lse_ref)) for _ in streams]
+    grads = [(torch.empty(qd.shape, dtype=torch.float32, device="cuda"),
+              torch.empty(kd.shape, dtype=torch.float32, device="cuda"),
+              torch.empty(kd.shape, dtype=torch.float32, device="cuda"),
+              torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")) for _ in streams]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for s, (o, l) in zip(streams, outs):
+            bd.bd_attn_fwd(plan, qd, kd, vd, o, l, stream=s)
+        torch.cuda.synchronize()
+        for o, l in outs:
+            assert torch.equal(o, out_ref) and torch.equal(l, lse_ref), f"forward, round {rep}"
+        for s, (dq, dk, dv, ws) in zip(streams, grads):
+            bd.bd_attn_bwd(plan, qd, kd, vd, out_ref, dod, lse_ref, dq, dk, dv, ws, stream=s)
+        torch.cuda.synchronize()
+        bd.bd_check_status(plan)
+        for dq, dk, dv, _ in grads[1:]:
+            assert torch.equal(dk, grads[0][1]) and torch.equal(dv, grads[0][2]), f"backward, round {rep}"
+            assert gu.max_rel(dq, grads[0][0]) < 1e-5
 
 
 def test_pre_without_clearing_after_caller_zeroes_dq():
