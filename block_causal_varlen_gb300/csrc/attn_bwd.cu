@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 8 * C_COUNT + 8);
   volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffBar + 8 * C_COUNT + 16);
-  int* claim = const_cast<int32_t*>(a.plan) + H_BWD_CLAIM;
+  int* claim = a.counters;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(512, 1)
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS, DEV_TIMEOUT);
       atomicExch(const_cast<int32_t*>(plan) + H_STATUS_DETAIL, 2);
     }
-    unit_counters_release(claim, const_cast<int32_t*>(plan) + H_BWD_DONE);
+    unit_counters_release(claim, claim + 1);
   }
 }
 
@@ -724,6 +724,7 @@ extern "C" int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_de
   p.lse2 = reinterpret_cast<float*>(wsb + c.ws.lse2);
   p.dstat = reinterpret_cast<float*>(wsb + c.ws.dstat);
   p.rowds = reinterpret_cast<int32_t*>(wsb + c.ws.rowds);
+  p.counters = reinterpret_cast<int32_t*>(wsb + c.ws.counters);
   p.dq = static_cast<float*>(dq->ptr);
   p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
   p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H; p.clear_dq = clear_dq ? 1 : 0;
@@ -789,6 +790,7 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   a.lse2 = reinterpret_cast<const float*>(wsb + c.ws.lse2);
   a.dstat = reinterpret_cast<const float*>(wsb + c.ws.dstat);
   a.rowds = reinterpret_cast<const int32_t*>(wsb + c.ws.rowds);
+  a.counters = reinterpret_cast<int32_t*>(wsb + c.ws.counters);
   a.dq = static_cast<float*>(dq->ptr);
   a.q_sb = dq->stride_b; a.q_sc = dq->stride_c; a.q_sr = dq->stride_row; a.q_sh = dq->stride_head;
   a.dk = static_cast<float*>(dk->ptr);
