@@ -297,13 +297,23 @@ def run_reference(args):
 
 
 def bench_workload(args):
-    """The workload `--workload` names, with `--head-dim` replacing its head dim."""
+    """The workload `--workload` names, with `--head-dim` replacing its head dim and,
+    for the single-document workload 4, `--seq-len` / `--cp` shrinking it (a reduced
+    case for profiler captures)."""
     import dataclasses
 
     import workloads
     wl = workloads.config(args.workload)
     if args.head_dim and args.head_dim != wl.d:
         wl = dataclasses.replace(wl, d=args.head_dim, name=wl.name.replace(f"_d{wl.d}", f"_d{args.head_dim}"))
+    if args.seq_len or args.cp:
+        if args.workload != 4:
+            raise SystemExit("--seq-len / --cp reshape only the single-document workload 4")
+        S = args.seq_len or wl.S
+        cp = args.cp or wl.cp
+        if S % cp or (S // cp) % 128:
+            raise SystemExit("--seq-len must be a multiple of 128 * cp")
+        wl = dataclasses.replace(wl, S=S, cp=cp, cu=[[0, S]], name=f"single_doc_s{S}_h{wl.H}kv{wl.Hkv}_d{wl.d}_cp{cp}")
     return wl
 
 
@@ -705,6 +715,9 @@ def main():
                     help="attention dropout probability (default 0, as in every benchmarked configuration)")
     ap.add_argument("--head-dim", type=int, default=0, choices=[0, 64, 128, 256],
                     help="replace the workload's head dim (default: keep it)")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="workload 4 only: the single document's length (a reduced case for profiler captures)")
+    ap.add_argument("--cp", type=int, default=0, help="workload 4 only: the number of chunks")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload block (the other workloads and head dim 256, timed after the headline)")
     ap.add_argument("--dq-in-fwd", action="store_true",

@@ -164,9 +164,9 @@ __global__ void __launch_bounds__(512, 1)
         }
         ++u;
         const StepRange<128> R{items, W[W_ITEM_LO], W[W_ITEM_HI], W[W_QLO], W[W_QHI], a.L};
-        // Q / dO / row statistics of a step are loaded once its stage is free, which
-        // is late (the stage's previous Q is read by the last MMA of the step before);
-        // so each step's tiles are first prefetched into L2 one step ahead
+        // Q / dO / row statistics of a step are loaded once its stage is free (the
+        // stage's previous Q is read by the last MMA of the step before); an L2
+        // prefetch of the next step's tiles measured no gain
         struct Step { int it, t, h, b, c; };
         Step prev{};
         bool have_prev = false;
@@ -585,19 +585,39 @@ __global__ void __launch_bounds__(512, 1)
         if (krow_ok) {
           float* row = x ? dkrow : dvrow;
           const float mul = x ? a.scale : 1.f;
+          if (a.rows32) {
+            // whole 32-byte sectors per store: the warp's 32 rows lie 4 KB or more apart
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q)
+            for (int q = 0; q < D / 32; ++q)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
-                                     __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
-              float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
-              if (a.accumulate) {
-                const float4 old = *p;
-                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              for (int e = 0; e < 4; ++e) {
+                float o[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[k] = __uint_as_float(v[q][8 * e + k]) * mul;
+                float* p = row + q * 32 + 8 * e;
+                if (a.accumulate) {
+                  float old[8];
+                  ld_global_v8(p, old);
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) o[k] += old[k];
+                }
+                st_global_v8(p, o);
               }
-              *p = o;
-            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
+                                       __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
+                float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
+                if (a.accumulate) {
+                  const float4 old = *p;
+                  o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                }
+                *p = o;
+              }
+          }
         }
       }
       ++u;
@@ -802,6 +822,13 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   a.work_off = owner ? pv.hdr(H_OFF_BWDO) : pv.hdr(H_OFF_BWD);
   a.ck_out = ck_out;
   a.accumulate = accumulate_dkv ? 1 : 0; a.dk_rows = dk->rows;
+  {
+    auto al32 = [](const bd_tensor* t) {
+      return reinterpret_cast<uintptr_t>(t->ptr) % 32 == 0 && (t->stride_b * 4) % 32 == 0 &&
+             (t->stride_c * 4) % 32 == 0 && (t->stride_row * 4) % 32 == 0 && (t->stride_head * 4) % 32 == 0;
+    };
+    a.rows32 = (al32(dk) && al32(dv)) ? 1 : 0;
+  }
   float scale;
   const int32_t sb = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &sb, 4);
