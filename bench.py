@@ -306,11 +306,12 @@ def bench_workload(args):
     wl = workloads.config(args.workload)
     if args.head_dim and args.head_dim != wl.d:
         wl = dataclasses.replace(wl, d=args.head_dim, name=wl.name.replace(f"_d{wl.d}", f"_d{args.head_dim}"))
-    if args.seq_len or args.cp:
+    seq_len, cp_arg = getattr(args, "seq_len", 0), getattr(args, "cp", 0)
+    if seq_len or cp_arg:
         if args.workload != 4:
             raise SystemExit("--seq-len / --cp reshape only the single-document workload 4")
-        S = args.seq_len or wl.S
-        cp = args.cp or wl.cp
+        S = seq_len or wl.S
+        cp = cp_arg or wl.cp
         if S % cp or (S // cp) % 128:
             raise SystemExit("--seq-len must be a multiple of 128 * cp")
         wl = dataclasses.replace(wl, S=S, cp=cp, cu=[[0, S]], name=f"single_doc_s{S}_h{wl.H}kv{wl.Hkv}_d{wl.d}_cp{cp}")
