@@ -63,33 +63,42 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   }
   __syncthreads();
   const int ds = s_ds;
-  const __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr;
-  const __nv_bfloat16* grow_p = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr;
-  const int npieces = a.H * CPH;
-  const int nround = (npieces + 255) & ~255;
-  for (int k0 = 0; k0 < nround; k0 += 256) {
-    const int k = k0 + tid;
-    const bool act = k < npieces;
-    const int h = k / CPH, col = (k % CPH) * 8;
-    float acc = 0.f;
-    if (act) {
-      const uint4 ov = *reinterpret_cast<const uint4*>(orow + int64_t(h) * a.o_sh + col);
-      const uint4 gv = *reinterpret_cast<const uint4*>(grow_p + int64_t(h) * a.g_sh + col);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
-        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-      }
-    }
-#pragma unroll
-    for (int off = CPH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (act && (k % CPH) == 0) {
+  if (ds < 0) {
+    // padding row: no attention, so D = 0 and the log2 LSE is +inf; O / dO are not read
+    for (int h = tid; h < a.H; h += blockDim.x) {
       const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
-      a.dstat[sidx] = ds >= 0 ? acc : 0.f;
-      const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
-      a.lse2[sidx] = ds >= 0 ? lse * 1.4426950408889634f : inf;
+      a.lse2[sidx] = inf;
+      a.dstat[sidx] = 0.f;
+    }
+  } else {
+    const __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr;
+    const __nv_bfloat16* grow_p = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr;
+    const int npieces = a.H * CPH;
+    const int nround = (npieces + 255) & ~255;
+    for (int k0 = 0; k0 < nround; k0 += 256) {
+      const int k = k0 + tid;
+      const bool act = k < npieces;
+      const int h = k / CPH, col = (k % CPH) * 8;
+      float acc = 0.f;
+      if (act) {
+        const uint4 ov = *reinterpret_cast<const uint4*>(orow + int64_t(h) * a.o_sh + col);
+        const uint4 gv = *reinterpret_cast<const uint4*>(grow_p + int64_t(h) * a.g_sh + col);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
+          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+      }
+#pragma unroll
+      for (int off = CPH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (act && (k % CPH) == 0) {
+        const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+        a.dstat[sidx] = acc;
+        const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
+        a.lse2[sidx] = lse * 1.4426950408889634f;
+      }
     }
   }
   if (!a.clear_dq) return;
