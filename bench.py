@@ -196,7 +196,9 @@ def tile_stats(plan, wl):
             dense += math.ceil(min(wl.S, c * wl.L + (t + 1) * 128) / 128)
     dense *= wl.B
     return {"visited_per_head": per_head, "dense_causal_per_head": dense,
-            "skipped_fraction": 1.0 - per_head / dense if dense else 0.0}
+            "skipped_fraction": 1.0 - per_head / dense if dense else 0.0,
+            # useful (query, key) pairs over the pairs of the visited tiles
+            "visited_density": plan.useful_pairs() / (per_head * 128 * 128) if per_head else 0.0}
 
 
 def useful_flops(plan, wl):
@@ -414,7 +416,7 @@ def workloads_block(bd, dev, flush, steps=20, warmup=3):
         out[wl.name] = {"fwd_ms": t_f, "fwd_bwd_ms": t_s, "fwd_tflops": f_fwd / (t_f * 1e-3) / 1e12,
                         "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_s * 1e-3) / 1e12, "useful_pairs": n_pairs,
                         "kv_mode": wl.kv_mode, "path": "owner-row backward" if fused else "backward",
-                        "steps": steps}
+                        "tiles": tile_stats(plan, wl), "steps": steps}
         del qd, dod, kd, vd, out_t, lse, dq, dk, dv, wsp, plan
         torch.cuda.empty_cache()
     return out
@@ -725,8 +727,8 @@ def main():
                     help="zero the fp32 dQ accumulator with the forward's idle warps (bd_attn_fwd_ex) instead of "
                          "in the backward's statistics kernel")
     ap.add_argument("--split", action="store_true",
-                    help="needed-only windows: time window partials + the owner-sum kernel and the statistics "
-                         "kernel clearing dQ, instead of the owner-row backward with dQ cleared by the forward")
+                    help="needed-only windows: time window partials + the owner-sum kernel instead of the "
+                         "owner-row backward")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
