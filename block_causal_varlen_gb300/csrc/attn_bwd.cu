@@ -372,13 +372,20 @@ __global__ void __launch_bounds__(512, 1)
               // (lanes are keys, so the whole-tile test differs across the warp: every
               // lane takes part in the shuffles whenever one of them masks)
               if (__any_sync(0xffffffffu, !full)) {
+                // key j sees the chunk's queries e in [elo, ehi): e >= j - (i0 + ib) for
+                // causality, and e < ehi where ehi counts the chunk's rows whose document
+                // starts at or before j (a prefix: the starts are non-decreasing and
+                // invalid rows, INT_MAX, come last), found by a binary search over the
+                // starts the lanes hold (lane l: row ib + l)
                 const int ds_mine = ch ? ds_mine1 : ds_mine0;
+                int ehi = 0;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  const int i = ib + e;
-                  const int ds_i = __shfl_sync(0xffffffffu, ds_mine, e);
-                  if (!full && !((j >= ds_i) && (j <= i0 + i))) p[e] = 0.f;
-                }
+                for (int step = 16; step >= 1; step >>= 1)
+                  if (__shfl_sync(0xffffffffu, ds_mine, ehi + step - 1) <= j) ehi += step;
+                if (__shfl_sync(0xffffffffu, ds_mine, ehi) <= j) ++ehi;
+                const int elo = j - (i0 + ib);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) p[e] = (e < elo || e >= ehi) ? 0.f : p[e];
               }
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[ch][e] = pack_bf16(p[2 * e], p[2 * e + 1]);
@@ -748,6 +755,13 @@ extern "C" int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_de
   p.dq = static_cast<float*>(dq->ptr);
   p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
   p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H; p.clear_dq = clear_dq ? 1 : 0;
+  p.rowds_off = c.pv.hdr(H_OFF_ROWDS);
+  {
+    // up to four 16-byte pieces per thread and block of 256: several rows per block
+    // when a row has few heads
+    const int pieces = c.H * (c.D / 8);
+    p.rows_per_block = pieces <= 256 ? 4 : pieces <= 512 ? 2 : 1;
+  }
   if ((st = launch_bwd_pre(p, c.D, static_cast<cudaStream_t>(stream)))) return st;
   return ok();
 }

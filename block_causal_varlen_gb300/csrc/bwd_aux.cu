@@ -33,85 +33,93 @@ BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
   return w;
 }
 
-// One block per (item, row < Lpad): D for every head, the log2-domain LSE, the
+// One block per `rows_per_block` consecutive rows (1, 2 or 4; they divide Lpad, so
+// a block's rows belong to one item): D for every head, the log2-domain LSE, the
 // row's document start, and (unless the caller cleared it already) zeroing of the
-// row's dQ accumulator. Threads take
-// 16-byte pieces of O / dO (all heads of the row); a head's pieces sit in
-// consecutive lanes and are summed with shuffles.
+// row's dQ accumulator. Threads take 16-byte pieces of O / dO of all heads of
+// the block's rows, up to four pieces each at a time, so that a thread keeps up
+// to 64 bytes of loads in flight; a head's pieces sit in consecutive lanes and
+// are summed with shuffles. Padding rows (no document) read nothing: their D is
+// 0 and their log2 LSE +inf.
 template <int D>
 __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
-  const int item = blockIdx.x / a.Lpad, l = blockIdx.x % a.Lpad;
+  constexpr int CPH = D / 8;  // 16-byte pieces per head (8, 16 or 32: groups never straddle a warp)
+  const int R = a.rows_per_block;
+  const int64_t grow0 = int64_t(blockIdx.x) * R;  // first row of the block in [nitems, Lpad]
+  const int item = int(grow0 / a.Lpad), l0 = int(grow0 % a.Lpad);
   const int b = item / a.C, c = item % a.C;
   const int tid = threadIdx.x;
   if (blockIdx.x == 0 && tid < 2) a.counters[tid] = 0;  // the main kernel's claim counters
-  constexpr int CPH = D / 8;  // 16-byte pieces per head (8, 16 or 32: groups never straddle a warp)
   const float inf = __int_as_float(0x7f800000);
-  if (l >= a.L) {
-    for (int h = tid; h < a.H; h += blockDim.x) {
-      const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
-      a.lse2[sidx] = inf;
-      a.dstat[sidx] = 0.f;
-    }
-    if (tid == 0) a.rowds[int64_t(item) * a.Lpad + l] = 0x7fffffff;
-    return;
-  }
-  __shared__ int s_ds;
-  if (tid == 0) {
-    const int32_t v = a.plan[a.plan[H_OFF_ROWDS] + item * a.L + l];
-    s_ds = v == kRowInvalid ? -1 : v;
+  __shared__ int s_ds[4];
+  if (tid < R) {
+    const int l = l0 + tid;
+    int32_t v = 0x7fffffff;
+    if (l < a.L) v = a.plan[a.rowds_off + int64_t(item) * a.L + l];
     a.rowds[int64_t(item) * a.Lpad + l] = v;
+    s_ds[tid] = v == kRowInvalid ? -1 : v;
+  }
+  if (a.clear_dq) {
+    const int per_row = a.H * (D / 4);
+    for (int f = tid; f < R * per_row; f += 256) {
+      const int r = f / per_row, k = f % per_row;
+      const int l = l0 + r;
+      if (l >= a.L) continue;
+      const int h = k / (D / 4), col = (k % (D / 4)) * 4;
+      float* p = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + col;
+      *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   __syncthreads();
-  const int ds = s_ds;
-  if (ds < 0) {
-    // padding row: no attention, so D = 0 and the log2 LSE is +inf; O / dO are not read
-    for (int h = tid; h < a.H; h += blockDim.x) {
-      const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
-      a.lse2[sidx] = inf;
-      a.dstat[sidx] = 0.f;
-    }
-  } else {
-    const __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr;
-    const __nv_bfloat16* grow_p = a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr;
-    const int npieces = a.H * CPH;
-    const int nround = (npieces + 255) & ~255;
-    for (int k0 = 0; k0 < nround; k0 += 256) {
-      const int k = k0 + tid;
-      const bool act = k < npieces;
-      const int h = k / CPH, col = (k % CPH) * 8;
-      float acc = 0.f;
-      if (act) {
-        const uint4 ov = *reinterpret_cast<const uint4*>(orow + int64_t(h) * a.o_sh + col);
-        const uint4 gv = *reinterpret_cast<const uint4*>(grow_p + int64_t(h) * a.g_sh + col);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+  const int npieces = a.H * CPH;  // per row
+  const int total = R * npieces;
+  for (int f0 = 0; f0 < total; f0 += 1024) {
+    uint4 ov[4], gv[4];
+    float lv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
-          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    for (int rr = 0; rr < 4; ++rr) {
+      const int f = f0 + rr * 256 + tid;
+      ov[rr] = gv[rr] = make_uint4(0u, 0u, 0u, 0u);
+      lv[rr] = 0.f;
+      if (f < total) {
+        const int r = f / npieces, k = f % npieces;
+        if (s_ds[r] >= 0) {
+          const int l = l0 + r, h = k / CPH, col = (k % CPH) * 8;
+          ov[rr] = *reinterpret_cast<const uint4*>(a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr +
+                                                   int64_t(h) * a.o_sh + col);
+          gv[rr] = *reinterpret_cast<const uint4*>(a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr +
+                                                   int64_t(h) * a.g_sh + col);
+          if (k % CPH == 0) lv[rr] = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
         }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      if (f0 + rr * 256 >= total) break;  // the same for the whole block: every lane shuffles
+      const int f = f0 + rr * 256 + tid;
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[rr]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[rr]);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
       }
 #pragma unroll
       for (int off = CPH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (act && (k % CPH) == 0) {
-        const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
-        a.dstat[sidx] = acc;
-        const float lse = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
-        a.lse2[sidx] = lse * 1.4426950408889634f;
+      if (f < total && (f % CPH) == 0) {
+        const int r = f / npieces, h = (f % npieces) / CPH;
+        const bool live = s_ds[r] >= 0;  // padding rows and rows past L: no attention
+        const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l0 + r;
+        a.dstat[sidx] = live ? acc : 0.f;
+        a.lse2[sidx] = live ? lv[rr] * 1.4426950408889634f : inf;
       }
     }
-  }
-  if (!a.clear_dq) return;
-  float* dqrow = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr;
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = tid; k < a.H * (D / 4); k += 256) {
-    const int h = k / (D / 4), col = (k % (D / 4)) * 4;
-    *reinterpret_cast<float4*>(dqrow + int64_t(h) * a.q_sh + col) = z;
   }
 }
 
 int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
-  const int64_t blocks = int64_t(a.nitems) * a.Lpad;
+  const int64_t blocks = int64_t(a.nitems) * a.Lpad / a.rows_per_block;
   if (blocks == 0) return BD_OK;
   if (blocks > 0x7fffffff) return fail(BD_ERR_UNSUPPORTED, "too many rows for the statistics kernel");
   if (D == 256) bd_bwd_pre_kernel<256><<<unsigned(blocks), 256, 0, s>>>(a);

@@ -320,16 +320,23 @@ int32_t build(const bd_plan_desc* d, Built* out) {
       if (lo < hi) *nq += (hi - 1 - I[I_ROW0]) / qstep - (lo - I[I_ROW0]) / qstep + 1;
     }
   };
-  // CTAs claim units in list order as they finish the previous one, so a list
-  // runs longest first (longest-processing-time order: the last units to start
-  // are the short ones); ties stay grouped by (K/V head, buffer), whose units
-  // read the same Q / dO tiles.
-  auto lpt_order = [](std::vector<BW>& v) {
-    std::stable_sort(v.begin(), v.end(), [](const BW& x, const BW& y) {
-      if (x.w[W_NQ] != y.w[W_NQ]) return x.w[W_NQ] > y.w[W_NQ];
-      if (x.w[W_G] != y.w[W_G]) return x.w[W_G] < y.w[W_G];
-      return x.w[W_OBUF] < y.w[W_OBUF];
-    });
+  // CTAs claim units in list order as they finish the previous one. A list runs
+  // longest first (longest-processing-time order: the last units to start are
+  // short ones, so the CTAs finish together), but only down to bands of similar
+  // length: within a band the units keep the order they are built in (K/V
+  // buffer, key tile, K/V head), so that the CTAs working at the same time hold
+  // neighbouring key tiles, whose steps read the same Q / dO tiles and add into
+  // the same dQ rows through L2. A band spans 1/kBandDiv of an even share of all
+  // steps over kOrderCtas CTAs (a GB300 runs one CTA per SM on its 152 SMs); the
+  // finishing spread this adds is at most one band. Layouts of short documents,
+  // whose units are all shorter than a band, run in position order.
+  constexpr int64_t kOrderCtas = 152, kBandDiv = 8;
+  auto lpt_order = [&](std::vector<BW>& v) {
+    int64_t total = 0;
+    for (const BW& x : v) total += x.w[W_NQ];
+    const int64_t band = std::max<int64_t>(1, total / (kOrderCtas * kBandDiv));
+    std::stable_sort(v.begin(), v.end(),
+                     [band](const BW& x, const BW& y) { return x.w[W_NQ] / band > y.w[W_NQ] / band; });
   };
   std::vector<BW> bw;
   for (int32_t nb = 0; nb < P.nbuf; ++nb) {
