@@ -94,7 +94,34 @@ enum : int {
   B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_TURN = 28, B_UFULL = 30,
   B_UEMPTY = 30 + kUnitSlots, B_COUNT = 30 + 2 * kUnitSlots
 };
-static_assert(8 * B_COUNT + 16 + 4 * kUnitSlots <= 512, "barriers, TMEM slot, abort flag and unit ring overflow their region");
+// Each slot of the forward's unit ring carries, besides the unit index, the unit's
+// words that the MMA and softmax warps need. The producer, which runs ahead of
+// them, reads these from global memory (a dependent chain: the unit, then its
+// item), so that a unit's first tile does not wait on those loads.
+enum : int { R_W = 0, R_NT, R_ITEM, R_QTILE, R_H0, R_KTLO, R_B, R_C, R_ROW0, kRingWords = 10 };
+static_assert(8 * B_COUNT + 16 + 4 * kUnitSlots * kRingWords <= 512,
+              "barriers, TMEM slot, abort flag and unit ring overflow their region");
+
+struct FwdUnit {
+  int w, nt, item, qtile, h0, ktlo, b, c, row0;
+};
+
+// Consumer side of ring entry k: every lane of a warp (or a lone thread with
+// one_thread set) copies the entry; one arrival per warp releases it. u.w is the
+// unit (-1: no more work, -2: the wait gave up).
+__device__ __forceinline__ void fwd_unit_take(uint32_t full0, uint32_t empty0, const volatile int32_t* ring,
+                                              uint32_t k, volatile int* abort, bool one_thread, FwdUnit& u) {
+  const int s = int(k % kUnitSlots);
+  const bool ok = mbar_wait(full0 + 8u * s, (k / kUnitSlots) & 1, abort);
+  const volatile int32_t* R = ring + s * kRingWords;
+  u.w = ok ? R[R_W] : -2;
+  if (u.w >= 0) {
+    u.nt = R[R_NT]; u.item = R[R_ITEM]; u.qtile = R[R_QTILE]; u.h0 = R[R_H0]; u.ktlo = R[R_KTLO];
+    u.b = R[R_B]; u.c = R[R_C]; u.row0 = R[R_ROW0];
+  }
+  if (!one_thread) __syncwarp();
+  if (ok && (one_thread || (threadIdx.x & 31) == 0)) mbar_arrive(empty0 + 8u * s);
+}
 
 template <int D, bool DROP>
 __global__ void __launch_bounds__(384, 1)
@@ -168,26 +195,39 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_v);
       uint32_t k_it = 0, v_it = 0, qi = 0;
       bool ok = true;
+      const int G = plan[H_G];
       for (uint32_t uk = 0; ok; ++uk) {
-        const int w = unit_publish(bar(B_UFULL), bar(B_UEMPTY), unit_ring, claim, a.n_work, uk, abort_flag);
-        if (w == -2) ok = false;
+        // claim the next unit and publish it with its words
+        const int us = int(uk % kUnitSlots);
+        if (!(ok = mbar_wait(bar(B_UEMPTY + us), ((uk / kUnitSlots) & 1) ^ 1, abort_flag))) break;
+        int w = atomicAdd(claim, 1);
+        if (w >= a.n_work) w = -1;
+        volatile int32_t* R = unit_ring + us * kRingWords;
+        int nt = 0, h0 = 0, qtile = 0, ktlo = 0, b = 0, c = 0, kvbuf = 0, kvbase = 0;
+        if (w >= 0) {
+          const int32_t* W = work + w * kFwdWords;
+          const int item = W[F_ITEM];
+          nt = W[F_NT]; h0 = W[F_H0]; qtile = W[F_QTILE]; ktlo = W[F_KTLO];
+          const int32_t* I = items + item * kItemWords;
+          b = I[I_B]; c = I[I_C]; kvbuf = I[I_KVBUF]; kvbase = I[I_KVBASE];
+          R[R_NT] = nt; R[R_ITEM] = item; R[R_QTILE] = qtile; R[R_H0] = h0; R[R_KTLO] = ktlo;
+          R[R_B] = b; R[R_C] = c; R[R_ROW0] = I[I_ROW0];
+        }
+        R[R_W] = w;
+        mbar_arrive(bar(B_UFULL + us));
         if (w < 0) break;
-        const int32_t* W = work + w * kFwdWords;
-        const int nt = W[F_NT];
         if (nt == 0) continue;
-        const int32_t* I = items + W[F_ITEM] * kItemWords;
-        const int b = I[I_B], c = I[I_C], kvbuf = I[I_KVBUF], kvbase = I[I_KVBASE];
-        const int g = W[F_H0] / (plan[H_G]);
+        const int g = h0 / G;
         const int kb = kvbuf / a.Ck, kc = kvbuf % a.Ck;
         if (!(ok = mbar_wait(bar(B_QEMPTY), (qi & 1) ^ 1, abort_flag))) break;
         mbar_expect_tx(bar(B_QFULL), slots * Cfg::kTileBytes);
         for (int s = 0; s < slots; ++s)
           for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_5d(sQ + s * Cfg::kTileBytes + hf * 16384, &tm_q, bar(B_QFULL), hf * 64, W[F_H0] + s,
-                        W[F_QTILE] * 128, c, b);
+            tma_load_5d(sQ + s * Cfg::kTileBytes + hf * 16384, &tm_q, bar(B_QFULL), hf * 64, h0 + s,
+                        qtile * 128, c, b);
         ++qi;
         for (int j = 0; j < nt; ++j) {
-          const int row = (W[F_KTLO] + j) * 128 - kvbase;
+          const int row = (ktlo + j) * 128 - kvbase;
           const int sk = k_it % NK, sv = v_it % NV;
           BD_TRACE_EVENT(24, int(k_it));  // producer: waits for a K stage
           if (!(ok = mbar_wait(bar(B_KEMPTY + sk), ((k_it / NK) & 1) ^ 1, abort_flag))) break;
@@ -269,10 +309,11 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t kv_it = 0, qi = 0, tcount = 0;
       bool ok = true;
       for (uint32_t uk = 0; ok; ++uk) {
-        const int w = unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, uk, abort_flag, true);
-        if (w == -2) ok = false;
-        if (w < 0) break;
-        const int nt = work[w * kFwdWords + F_NT];
+        FwdUnit U;
+        fwd_unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, uk, abort_flag, true, U);
+        if (U.w == -2) ok = false;
+        if (U.w < 0) break;
+        const int nt = U.nt;
         if (nt == 0) continue;
         if (!(ok = mbar_wait(bar(B_QFULL), qi & 1, abort_flag))) break;
         {
@@ -364,19 +405,26 @@ __global__ void __launch_bounds__(384, 1)
     if (s < slots) {
       uint32_t tcount = 0, qi = 0;
       bool ok = true;
+      // The next unit is taken from the ring, and the load of its rows' document
+      // starts issued, before this unit's epilogue, whose stores hide that load
+      FwdUnit U;
+      int ds_u = kRowInvalid;
+      auto take = [&](uint32_t k, FwdUnit& X, int& dsx) {
+        fwd_unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, k, abort_flag, false, X);
+        dsx = kRowInvalid;
+        if (X.w >= 0 && X.qtile * 128 + r < a.L) dsx = rowds_all[X.item * a.L + X.qtile * 128 + r];
+      };
+      take(0, U, ds_u);
       for (uint32_t uk = 0; ok; ++uk) {
-        const int w = unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, uk, abort_flag, false);
-        if (w == -2) ok = false;
-        if (w < 0) break;
-        const int32_t* W = work + w * kFwdWords;
-        const int nt = W[F_NT];
-        const int32_t* I = items + W[F_ITEM] * kItemWords;
-        const int b = I[I_B], c = I[I_C];
-        const int h = W[F_H0] + s;
-        const int lrow = W[F_QTILE] * 128 + r;  // row within the chunk
-        const int grow = I[I_ROW0] + lrow;      // global row
+        if (U.w == -2) ok = false;
+        if (U.w < 0) break;
+        const int nt = U.nt;
+        const int b = U.b, c = U.c;
+        const int h = U.h0 + s;
+        const int lrow = U.qtile * 128 + r;  // row within the chunk
+        const int grow = U.row0 + lrow;      // global row
         const bool row_ok = lrow < a.L;
-        const int ds = row_ok ? rowds_all[W[F_ITEM] * a.L + lrow] : kRowInvalid;
+        const int ds = ds_u;
         const bool valid = ds != kRowInvalid;
         (void)grow;
         __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(lrow) * a.o_sr + int64_t(h) * a.o_sh;
@@ -388,6 +436,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; k < D / 8; ++k) reinterpret_cast<uint4*>(orow)[k] = z;
             *lrow_p = -CUDART_INF_F;
           }
+          take(uk + 1, U, ds_u);
           continue;
         }
         float m_run = -CUDART_INF_F, l_run = 0.f;
@@ -407,13 +456,21 @@ __global__ void __launch_bounds__(384, 1)
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[q][e]);
-          const int c0 = (W[F_KTLO] + j) * 128;
-          const bool full = valid && c0 >= ds && c0 + 127 <= grow;
-          if (!full) {
+          // the row sees the tile's columns [lo, hi] (none when the row is invalid)
+          const int c0 = (U.ktlo + j) * 128;
+          const int lo = valid ? ds - c0 : 128, hi = valid ? grow - c0 : -1;
+          if (__any_sync(0xffffffffu, !(lo <= 0 && hi >= 127))) {
+            // 32-column groups that every row of the warp sees whole are left alone,
+            // groups no row sees are cleared; only the rest is masked per element
 #pragma unroll
-            for (int e = 0; e < 128; ++e) {
-              const int col = c0 + e;
-              if (!(valid && col >= ds && col <= grow)) x[e] = -CUDART_INF_F;
+            for (int q = 0; q < 4; ++q) {
+              const bool seen = lo <= 32 * q && hi >= 32 * q + 31, unseen = hi < 32 * q || lo > 32 * q + 31;
+              if (!__all_sync(0xffffffffu, seen)) {
+                const bool clear = __all_sync(0xffffffffu, unseen);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  x[32 * q + e] = (clear || 32 * q + e < lo || 32 * q + e > hi) ? -CUDART_INF_F : x[32 * q + e];
+              }
             }
           }
           // row max: eight independent 3-input max chains, then a small tree
@@ -457,7 +514,7 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t kbits[4] = {0u, 0u, 0u, 0u};
           if constexpr (DROP) {
             const uint32_t T = a.drop_thresh, kb0 = uint32_t(c0) >> 1, rb = uint32_t(grow) >> 1;
-            if ((I[I_ROW0] & 1) == 0) {
+            if ((U.row0 & 1) == 0) {
               // rows 2m, 2m + 1 are lanes 2m, 2m + 1: each lane makes every other call
               // of the pair and hands its partner the two words the partner needs
               const uint32_t odd = lane & 1;
@@ -510,29 +567,60 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) BD_TRACE_EVENT(4 * s + quarter, int(tcount));  // per warp: P stored
         }
         if (!ok) break;
+        FwdUnit N;
+        int ds_n;
+        take(uk + 1, N, ds_n);
         if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
         tc_fence_after();
         const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * (DROP ? a.drop_scale : 1.f);
-#pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t ov[32];
-          tmem_ld32(tO + q * 32, ov);
+        if constexpr (D <= 128) {
+          // the whole O row leaves TMEM first, so that the next unit's first PV may
+          // overwrite the accumulator while the row is stored
+          uint32_t ov[D / 32][32];
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + q * 32, ov[q]);
           tmem_ld_wait();
-          reg_fence(ov);
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+          for (int q = 0; q < D / 32; ++q) reg_fence(ov[q]);
+          tc_fence_before();
+          mbar_arrive(bar(B_OEMPTY + s));
 #pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(__uint_as_float(ov[q][2 * e]) * inv, __uint_as_float(ov[q][2 * e + 1]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
           }
+          if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
+        } else {
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(tO + q * 32, ov);
+            tmem_ld_wait();
+            reg_fence(ov);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
+          }
+          if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
+          tc_fence_before();
+          mbar_arrive(bar(B_OEMPTY + s));
         }
-        if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
-        tc_fence_before();
-        mbar_arrive(bar(B_OEMPTY + s));
         ++qi;
+        U = N;
+        ds_u = ds_n;
       }
     }
   }
