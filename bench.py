@@ -401,10 +401,14 @@ def workloads_block(bd, dev, flush, steps=20, warmup=3):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             flush.zero_()
             ev[0].record(stream)
-            bd.bd_attn_fwd(plan, qd, kd, vd, out_t, lse, stream=stream)
+            if with_bwd:  # the forward's idle warp zeroes the backward's dQ accumulator
+                bd.bd_attn_fwd_ex(plan, qd, kd, vd, out_t, lse, dq_zero=dq, stream=stream)
+            else:
+                bd.bd_attn_fwd(plan, qd, kd, vd, out_t, lse, stream=stream)
             ev[1].record(stream)
             if with_bwd:
-                bd.bd_attn_bwd_ex(plan, qd, kd, vd, out_t, dod, lse, dq, dk, dv, wsp, flags, stream=stream)
+                bd.bd_attn_bwd_ex(plan, qd, kd, vd, out_t, dod, lse, dq, dk, dv, wsp,
+                                  flags | bd.BD_BWD_DQ_ZEROED, stream=stream)
             ev[2].record(stream)
             return ev
 
@@ -415,7 +419,8 @@ def workloads_block(bd, dev, flush, steps=20, warmup=3):
         t_s = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
         out[wl.name] = {"fwd_ms": t_f, "fwd_bwd_ms": t_s, "fwd_tflops": f_fwd / (t_f * 1e-3) / 1e12,
                         "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_s * 1e-3) / 1e12, "useful_pairs": n_pairs,
-                        "kv_mode": wl.kv_mode, "path": "owner-row backward" if fused else "backward",
+                        "kv_mode": wl.kv_mode,
+                        "path": ("owner-row backward" if fused else "backward") + "; dQ zeroed by the forward",
                         "tiles": tile_stats(plan, wl), "steps": steps}
         del qd, dod, kd, vd, out_t, lse, dq, dk, dv, wsp, plan
         torch.cuda.empty_cache()
@@ -477,10 +482,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     # needed-only windows over every chunk: dK / dV summed at their owners inside the
-    # backward kernel (no owner-sum kernel); --dq-in-fwd also moves the zeroing of dQ
-    # from the statistics kernel to the forward's otherwise idle warps
+    # backward kernel (no owner-sum kernel). The forward's otherwise idle warp 3 zeroes
+    # the fp32 dQ accumulator (bd_attn_fwd_ex); --dq-in-pre moves that back to the
+    # statistics kernel
     fused = (not args.split) and mode == bd.BD_KV_WINDOW and plan.owner_units() > 0
-    zero_in_fwd = args.dq_in_fwd
+    zero_in_fwd = not args.dq_in_pre
     launches_per_step = 3 if fused else 3 + (1 if mode == bd.BD_KV_WINDOW else 0)
 
     def step(ev):
@@ -567,8 +573,10 @@ def run_ours(args):
                         dk=torch.zeros_like(dk_own), dv=torch.zeros_like(dv_own),
                         ws=torch.empty_like(wsp))
             sets.append(dset)
-        # the plan blob goes up once per step too (host build stays outside: it is the same blob every step)
+        # the plan blob goes up once per step too (host build stays outside: it is the same blob every step),
+        # with the step's inputs, into the buffer set's own device copy of the plan
         plan_pinned = torch.from_numpy(plan.host).pin_memory()
+        plans = [bd.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, wl.d, kv_mode=mode).upload(dev) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host_in[0].values()) + plan_pinned.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -582,27 +590,28 @@ def run_ours(args):
         def e2e_step(t):
             i = t % 2
             D_, Hi, Ho = sets[i], host_in[i], host_out[i]
+            P_ = plans[i]
             with torch.cuda.stream(s_in):
                 s_in.wait_event(comp_done[i])            # step t-2 finished reading this set
+                P_.dev.copy_(plan_pinned, non_blocking=True)
                 for key in ("q", "k", "v", "do"):
                     D_[key].copy_(Hi[key], non_blocking=True)
                 in_ready[i].record(s_in)
             stream.wait_event(in_ready[i])
             stream.wait_event(out_done[i])               # step t-2's results have left this set
-            plan.dev.copy_(plan_pinned, non_blocking=True)  # on the compute stream: after the last step's kernels
             if zero_in_fwd:
-                bd.bd_attn_fwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], dq_zero=D_["dq"], stream=stream)
+                bd.bd_attn_fwd_ex(P_, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], dq_zero=D_["dq"], stream=stream)
             else:
-                bd.bd_attn_fwd(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
+                bd.bd_attn_fwd(P_, D_["q"], D_["k"], D_["v"], D_["o"], D_["l"], stream=stream)
             zflag = bd.BD_BWD_DQ_ZEROED if zero_in_fwd else 0
             if fused:
-                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dk"],
+                bd.bd_attn_bwd_ex(P_, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dk"],
                                   D_["dv"], D_["ws"], bd.BD_BWD_OWNER_ROWS | zflag, stream=stream)
             else:
-                bd.bd_attn_bwd_ex(plan, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
+                bd.bd_attn_bwd_ex(P_, D_["q"], D_["k"], D_["v"], D_["o"], D_["do"], D_["l"], D_["dq"], D_["dkw"],
                                   D_["dvw"], D_["ws"], zflag, stream=stream)
                 if mode == bd.BD_KV_WINDOW:
-                    bd.bd_owner_sum(plan, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream,
+                    bd.bd_owner_sum(P_, D_["dkw"], D_["dvw"], D_["dk"], D_["dv"], stream=stream,
                                     accumulate=False)
             comp_done[i].record(stream)
             with torch.cuda.stream(s_out):
@@ -623,6 +632,8 @@ def run_ours(args):
         stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        for P_ in plans:
+            bd.bd_check_status(P_)
         te = e0.elapsed_time(e1) / n_e2e
         e2e = {"value": ws * f_step / (te * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": te, "steps": n_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -723,9 +734,9 @@ def main():
     ap.add_argument("--cp", type=int, default=0, help="workload 4 only: the number of chunks")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload block (the other workloads and head dim 256, timed after the headline)")
-    ap.add_argument("--dq-in-fwd", action="store_true",
-                    help="zero the fp32 dQ accumulator with the forward's idle warps (bd_attn_fwd_ex) instead of "
-                         "in the backward's statistics kernel")
+    ap.add_argument("--dq-in-pre", action="store_true",
+                    help="zero the fp32 dQ accumulator in the backward's statistics kernel instead of with the "
+                         "forward's idle warp (bd_attn_fwd_ex, the default)")
     ap.add_argument("--split", action="store_true",
                     help="needed-only windows: time window partials + the owner-sum kernel instead of the "
                          "owner-row backward")

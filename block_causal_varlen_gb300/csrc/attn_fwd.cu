@@ -75,7 +75,9 @@ struct FwdCfg {
   static constexpr int kOffK = kOffQ + kQSlots * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-  static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
+  // the 128 rows' document starts of a unit's query tile, two buffers (units in turn)
+  static constexpr int kOffDs = kOffBar + 512;
+  static constexpr int kSmem = kOffDs + 2 * 512 + 1024;  // + alignment slack
   static constexpr int kOCol = 256;                   // first O column in TMEM
   static constexpr int kThreads = 384;
   // register split after setmaxnreg: warpgroup 0 (producer, MMA) and the two
@@ -91,8 +93,8 @@ struct FwdCfg {
 // barrier indices (8 bytes each)
 enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14, B_SFULL = 18,
-  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_TURN = 28, B_UFULL = 30,
-  B_UEMPTY = 30 + kUnitSlots, B_COUNT = 30 + 2 * kUnitSlots
+  B_PFULL = 20, B_OFINAL = 22, B_OEMPTY = 24, B_DRAIN = 26, B_TURN = 28, B_DSFULL = 30, B_UFULL = 32,
+  B_UEMPTY = 32 + kUnitSlots, B_COUNT = 32 + 2 * kUnitSlots
 };
 // Each slot of the forward's unit ring carries, besides the unit index, the unit's
 // words that the MMA and softmax warps need. The producer, which runs ahead of
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + Cfg::kOffQ, sK = sbase + Cfg::kOffK, sV = sbase + Cfg::kOffV;
+  const uint32_t sDs = sbase + Cfg::kOffDs;
   const uint32_t bars = sbase + Cfg::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 8 * B_COUNT);
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(384, 1)
   const int32_t* plan = a.plan;
   const int32_t* work = plan + plan[H_OFF_FWD];
   const int32_t* items = plan + plan[H_OFF_ITEMS];
-  const int32_t* rowds_all = plan + plan[H_OFF_ROWDS];
+  const int32_t* rowds_all = plan + plan[H_OFF_ROWDS];  // [nitems][Lpad]
+  const int Lpad = plan[H_QTILES] * 128;
   const int slots = a.slots;
 
   if (threadIdx.x == 0) {
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(B_VEMPTY + s), slots);
     }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_DSFULL + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_PFULL + s), 128);
       mbar_init(bar(B_OFINAL + s), 1);
@@ -203,10 +208,10 @@ __global__ void __launch_bounds__(384, 1)
         int w = atomicAdd(claim, 1);
         if (w >= a.n_work) w = -1;
         volatile int32_t* R = unit_ring + us * kRingWords;
-        int nt = 0, h0 = 0, qtile = 0, ktlo = 0, b = 0, c = 0, kvbuf = 0, kvbase = 0;
+        int nt = 0, h0 = 0, qtile = 0, ktlo = 0, b = 0, c = 0, kvbuf = 0, kvbase = 0, item = 0;
         if (w >= 0) {
           const int32_t* W = work + w * kFwdWords;
-          const int item = W[F_ITEM];
+          item = W[F_ITEM];
           nt = W[F_NT]; h0 = W[F_H0]; qtile = W[F_QTILE]; ktlo = W[F_KTLO];
           const int32_t* I = items + item * kItemWords;
           b = I[I_B]; c = I[I_C]; kvbuf = I[I_KVBUF]; kvbase = I[I_KVBASE];
@@ -225,6 +230,11 @@ __global__ void __launch_bounds__(384, 1)
           for (int hf = 0; hf < D / 64; ++hf)
             tma_load_5d(sQ + s * Cfg::kTileBytes + hf * 16384, &tm_q, bar(B_QFULL), hf * 64, h0 + s,
                         qtile * 128, c, b);
+        // the tile rows' document starts for the softmax warps (buffer qi & 1 was
+        // last read at the start of unit qi - 2, before that unit's first P and so
+        // before the S that released the Q stage just waited for)
+        mbar_expect_tx(bar(B_DSFULL + (qi & 1)), 512);
+        bulk_load(sDs + (qi & 1) * 512, rowds_all + int64_t(item) * Lpad + qtile * 128, 512, bar(B_DSFULL + (qi & 1)));
         ++qi;
         for (int j = 0; j < nt; ++j) {
           const int row = (ktlo + j) * 128 - kvbase;
@@ -260,6 +270,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait_drain(bar(B_VFULL + s), (last / NV) & 1);
           }
         if (qi > 0) mbar_wait_drain(bar(B_QFULL), (qi - 1) & 1);
+        for (uint32_t x = (qi > 2 ? qi - 2 : 0); x < qi; ++x) mbar_wait_drain(bar(B_DSFULL + (x & 1)), (x >> 1) & 1);
       }
     }
   } else if (warp == 1 || (warp == 2 && slots == 2)) {
@@ -363,19 +374,18 @@ __global__ void __launch_bounds__(384, 1)
     }
    }
    else if (warp == 3) {
-    // warp 3: zero the caller's dQ accumulator (one d-vector of one (row, head)
-    // per warp store round), spread over every CTA of the launch
+    // warp 3: zero the caller's dQ accumulator, one (row, head) d-vector per warp
+    // store round, rows spread over every CTA of the launch (32-bit index
+    // arithmetic once per row)
     if (a.dqz != nullptr) {
-      const int64_t nvec = int64_t(a.B) * a.C * a.L * a.H;
-      for (int64_t vid = blockIdx.x; vid < nvec; vid += gridDim.x) {
-        const int h = int(vid % a.H);
-        const int64_t r = vid / a.H;
-        const int l = int(r % a.L);
-        const int64_t bc = r / a.L;
-        float* p = a.dqz + (bc / a.C) * a.z_sb + (bc % a.C) * a.z_sc + int64_t(l) * a.z_sr + int64_t(h) * a.z_sh;
+      const int rows = a.B * a.C * a.L;
+      for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int l = row % a.L, bc = row / a.L;
+        float* p = a.dqz + int64_t(bc / a.C) * a.z_sb + int64_t(bc % a.C) * a.z_sc + int64_t(l) * a.z_sr;
+        for (int h = 0; h < a.H; ++h)
 #pragma unroll
-        for (int col = lane * 4; col < D; col += 128)
-          *reinterpret_cast<float4*>(p + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int col = lane * 4; col < D; col += 128)
+            *reinterpret_cast<float4*>(p + int64_t(h) * a.z_sh + col) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #ifdef BD_TRACE
@@ -405,16 +415,13 @@ __global__ void __launch_bounds__(384, 1)
     if (s < slots) {
       uint32_t tcount = 0, qi = 0;
       bool ok = true;
-      // The next unit is taken from the ring, and the load of its rows' document
-      // starts issued, before this unit's epilogue, whose stores hide that load
+      // the next unit is taken from the ring before this unit's epilogue
       FwdUnit U;
-      int ds_u = kRowInvalid;
-      auto take = [&](uint32_t k, FwdUnit& X, int& dsx) {
+      auto take = [&](uint32_t k, FwdUnit& X) {
         fwd_unit_take(bar(B_UFULL), bar(B_UEMPTY), unit_ring, k, abort_flag, false, X);
-        dsx = kRowInvalid;
-        if (X.w >= 0 && X.qtile * 128 + r < a.L) dsx = rowds_all[X.item * a.L + X.qtile * 128 + r];
       };
-      take(0, U, ds_u);
+      const int32_t* ds_buf = reinterpret_cast<const int32_t*>(smem + Cfg::kOffDs);
+      take(0, U);
       for (uint32_t uk = 0; ok; ++uk) {
         if (U.w == -2) ok = false;
         if (U.w < 0) break;
@@ -424,7 +431,13 @@ __global__ void __launch_bounds__(384, 1)
         const int lrow = U.qtile * 128 + r;  // row within the chunk
         const int grow = U.row0 + lrow;      // global row
         const bool row_ok = lrow < a.L;
-        const int ds = ds_u;
+        // the row's document start, loaded with the unit's Q tile (rows past L are
+        // invalid); not needed by a unit without tiles
+        int ds = kRowInvalid;
+        if (nt > 0) {
+          if (!(ok = mbar_wait(bar(B_DSFULL + (qi & 1)), (qi >> 1) & 1, abort_flag))) break;
+          ds = ds_buf[(qi & 1) * 128 + r];
+        }
         const bool valid = ds != kRowInvalid;
         (void)grow;
         __nv_bfloat16* orow = a.o + b * a.o_sb + c * a.o_sc + int64_t(lrow) * a.o_sr + int64_t(h) * a.o_sh;
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; k < D / 8; ++k) reinterpret_cast<uint4*>(orow)[k] = z;
             *lrow_p = -CUDART_INF_F;
           }
-          take(uk + 1, U, ds_u);
+          take(uk + 1, U);
           continue;
         }
         float m_run = -CUDART_INF_F, l_run = 0.f;
@@ -459,28 +472,36 @@ __global__ void __launch_bounds__(384, 1)
           // the row sees the tile's columns [lo, hi] (none when the row is invalid)
           const int c0 = (U.ktlo + j) * 128;
           const int lo = valid ? ds - c0 : 128, hi = valid ? grow - c0 : -1;
+          // Per 32-column group, for the whole warp: bit q of `gone` is set when no row
+          // sees any column of group q (cleared without tests, left out of the row
+          // max); groups every row sees whole are left alone; only the others are
+          // masked element by element.
+          uint32_t gone = 0;
           if (__any_sync(0xffffffffu, !(lo <= 0 && hi >= 127))) {
-            // 32-column groups that every row of the warp sees whole are left alone,
-            // groups no row sees are cleared; only the rest is masked per element
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const bool seen = lo <= 32 * q && hi >= 32 * q + 31, unseen = hi < 32 * q || lo > 32 * q + 31;
-              if (!__all_sync(0xffffffffu, seen)) {
-                const bool clear = __all_sync(0xffffffffu, unseen);
+              if (__all_sync(0xffffffffu, hi < 32 * q || lo > 32 * q + 31)) {
+                gone |= 1u << q;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[32 * q + e] = -CUDART_INF_F;
+              } else if (!__all_sync(0xffffffffu, lo <= 32 * q && hi >= 32 * q + 31)) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                  x[32 * q + e] = (clear || 32 * q + e < lo || 32 * q + e > hi) ? -CUDART_INF_F : x[32 * q + e];
+                  x[32 * q + e] = (32 * q + e < lo || 32 * q + e > hi) ? -CUDART_INF_F : x[32 * q + e];
               }
             }
           }
           // row max: eight independent 3-input max chains, then a small tree
           float m8[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(x[k], x[8 + k]);
+          for (int k = 0; k < 8; ++k) m8[k] = -CUDART_INF_F;
 #pragma unroll
-          for (int e = 16; e < 128; e += 16)
+          for (int q = 0; q < 4; ++q)
+            if (!(gone & (1u << q)))
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], x[e + k], x[e + 8 + k]);
+              for (int e = 32 * q; e < 32 * q + 32; e += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], x[e + k], x[e + 8 + k]);
           const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
           if (r == 0) BD_TRACE_EVENT(40 + s, int(tcount));  // softmax: row max done
           const float m_new = fmaxf(m_run, mx * a.scale_log2);
@@ -568,8 +589,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (!ok) break;
         FwdUnit N;
-        int ds_n;
-        take(uk + 1, N, ds_n);
+        take(uk + 1, N);
         if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
         tc_fence_after();
         const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * (DROP ? a.drop_scale : 1.f);
@@ -620,7 +640,6 @@ __global__ void __launch_bounds__(384, 1)
         }
         ++qi;
         U = N;
-        ds_u = ds_n;
       }
     }
   }

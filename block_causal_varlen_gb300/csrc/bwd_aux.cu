@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
   if (tid < R) {
     const int l = l0 + tid;
     int32_t v = 0x7fffffff;
-    if (l < a.L) v = a.plan[a.rowds_off + int64_t(item) * a.L + l];
+    if (l < a.L) v = a.plan[a.rowds_off + int64_t(item) * a.Lpad + l];
     a.rowds[int64_t(item) * a.Lpad + l] = v;
     s_ds[tid] = v == kRowInvalid ? -1 : v;
   }

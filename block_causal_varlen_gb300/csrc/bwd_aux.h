@@ -21,7 +21,7 @@ struct BwdPreArgs {
   float* dq;       // zeroed when clear_dq is set
   int64_t q_sb, q_sc, q_sr, q_sh;
   int32_t nitems, C, L, Lpad, H, clear_dq;
-  int32_t rowds_off;       // word offset of the plan's per-row document starts ([nitems, L])
+  int32_t rowds_off;       // word offset of the plan's per-row document starts ([nitems, Lpad])
   int32_t rows_per_block;  // 1, 2 or 4 rows per block (set by launch_bwd_pre's caller)
 };
 

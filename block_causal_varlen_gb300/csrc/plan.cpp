@@ -58,7 +58,7 @@ int32_t view_plan(const void* plan_host, PlanView* out) {
   if (!in(w[H_OFF_ITEMS], w[H_NITEMS], kItemWords) || !in(w[H_OFF_SEGS], w[H_NSEGS], kSegWords) ||
       !in(w[H_OFF_FWD], w[H_NFWD], kFwdWords) || !in(w[H_OFF_BWD], w[H_NBWD], kBwdWords) ||
       (w[H_NBWDO] != 0 && !in(w[H_OFF_BWDO], w[H_NBWDO], kBwdWords)) ||
-      !in(w[H_OFF_ROWDS], w[H_NITEMS], w[H_L]))
+      !in(w[H_OFF_ROWDS], w[H_NITEMS], int64_t(w[H_QTILES]) * kTile))
     return fail(BD_ERR_PLAN, "plan blob offsets are inconsistent");
   out->w = w;
   return BD_OK;
@@ -258,10 +258,12 @@ int32_t build(const bd_plan_desc* d, Built* out) {
         P.segs.insert(P.segs.end(), w, w + kSegWords);
       }
       P.kv_rows = std::max(P.kv_rows, d->kv_mode == BD_KV_GATHER ? h.s_valid : h.kv_end - h.kv_start);
-      // per-row document start: segments cover the chunk's valid rows in order
+      // per-row document start: segments cover the chunk's valid rows in order; an
+      // item's rows take Lpad words (rows past L are invalid), so that a query
+      // tile's 128 starts are one aligned 512-byte block
       {
         const size_t base = P.rowds.size();
-        P.rowds.resize(base + L, kRowInvalid);
+        P.rowds.resize(base + size_t(P.qtiles) * kTile, kRowInvalid);
         for (int32_t s = 0; s < h.nseg; ++s)
           for (int32_t r = tmp[s].q_start; r < tmp[s].q_start + tmp[s].q_len; ++r)
             P.rowds[base + (r - h.row_offset)] = tmp[s].k_start;

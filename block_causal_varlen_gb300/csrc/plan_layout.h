@@ -16,7 +16,7 @@ enum : int {
   H_KVMODE, H_G, H_NITEMS, H_OFF_ITEMS, H_OFF_SEGS, H_NSEGS, H_OFF_FWD, H_NFWD,
   H_OFF_BWD, H_NBWD, H_SCALE_BITS, H_KV_ROWS, H_CK, H_SLOTS, H_QTILES,
   H_USEFUL_LO, H_USEFUL_HI, H_NBUF, H_FWD_TILES_LO, H_FWD_TILES_HI,
-  H_OFF_ROWDS,          // int32 [nitems][L]: global start row of each chunk row's
+  H_OFF_ROWDS,          // int32 [nitems][Lpad]: global start row of each chunk row's
                         // document, kRowInvalid for padding rows
   H_DROP_THRESH,        // attention dropout: keep iff Philox word >= this (uint32; 0 = off)
   H_DROP_SCALE_BITS,    // 1 / (1 - p) as float bits
