@@ -811,7 +811,7 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   // dQ reduce boxes: 128 rows x 32 columns (128-byte swizzle), or at head dim 256
   // (transposed dQ) 16 rows x 32 columns; Q / dO boxes are one backward query
   // step high
-  if ((st = c.D == 256 ? make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 16)
+  if ((st = c.D == 256 ? make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 128, 16)
                        : make_tmap_f32_reduce(&mdq, dq, c.B, c.C, c.H, c.D, "dq", 32, 128)))
     return st;
   if ((st = make_tmap_bf16(&mq, q, c.B, c.C, c.H, c.D, "q", bwd_query_step(c.D)))) return st;

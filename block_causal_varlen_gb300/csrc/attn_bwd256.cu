@@ -25,8 +25,9 @@
 //   warps 4-11   P^T (pass 0, into TMEM for the dV product) and dS^T (pass 1,
 //                into shared memory), lane = key row, 32 queries per warp.
 //   warps 12-15  pass 1: read dQ^T (lane = column of d) out of TMEM, transpose it
-//                through per-warp staging boxes and add it into dQ with TMA
-//                reduce-adds; end of each pass: write dV, then dK (x scale).
+//                through two shared staging boxes (16 query rows x one d half)
+//                and add it into dQ with TMA reduce-adds; end of each pass:
+//                write dV, then dK (x scale).
 // TMEM columns: S^T [0, 64), dP^T [64, 128), dQ^T [128, 256), dV / dK [256, 512).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,7 +49,7 @@ struct Cfg256 {
   static constexpr int kOffK = 0, kOffV = kKVBytes, kOffQ = 2 * kKVBytes;
   static constexpr int kOffDO = kOffQ + kQBytes;
   static constexpr int kOffDS = kOffDO + kQBytes;      // dS^T: 128 keys x 64 queries bf16
-  static constexpr int kOffStage = kOffDS + 128 * QR * 2;  // dQ staging: 2 x 2 KB per dQ warp
+  static constexpr int kOffStage = kOffDS + 128 * QR * 2;  // dQ staging: two 16-row x 128-column fp32 boxes
   static constexpr int kStageBytes = 16384;
   static constexpr int kOffStat = kOffStage + kStageBytes;  // two stages: lse2, D, ds of 64 rows
   static constexpr int kStatBytes = 3 * QR * 4;
@@ -482,8 +483,8 @@ __global__ void __launch_bounds__(512, 1)
               for (int h2 = 0; h2 < a.G && ok; ++h2, ++s1) {
                 const int t = t1 - tt, hh = a.G - 1 - h2;
                 const int h = g * a.G + hh;
-                // lanes of a warp leave together (they meet at __syncwarp below)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(E_DQFULL), s1 & 1, abort_flag));
+                // the four dQ warps leave together (they meet at named barriers below)
+                ok = bar_red_and(1, 128, mbar_wait(bar(E_DQFULL), s1 & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 // r[2 dh + k]: column 128 dh + rl of dQ^T, query rows 32 k .. 32 k + 31
@@ -495,25 +496,27 @@ __global__ void __launch_bounds__(512, 1)
                 for (int q = 0; q < 4; ++q) reg_fence(r[q]);
                 tc_fence_before();
                 mbar_arrive(bar(E_DQEMPTY));
-                // row-major 16-row x 32-column boxes (128-byte rows, 128-byte swizzle:
-                // 16-byte piece c of row q sits at c ^ (q & 7)) in this warp's two
-                // buffers, each sent with a TMA reduce-add (rows past L are clipped)
+                // 16-row x 128-column boxes (one d half, 8 KB, row-major, unswizzled:
+                // each warp writes its 32 columns of a row as one 128-byte run) built
+                // by the four warps together in two buffers, each sent with one TMA
+                // reduce-add (rows past L are clipped). An SM's reduce-adds proceed one
+                // box at a time at about the same cost up to 8 KB, so four warps
+                // sending 2 KB boxes of 32 columns took four times as long.
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                   const int dh = k >> 2, rr = k & 3;
-                  const uint32_t buf = sStage + (quarter * 2 + (k & 1)) * 2048;
-                  if (lane == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
-                  __syncwarp();
+                  const uint32_t buf = sStage + (k & 1) * 8192;
+                  if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
+                  named_bar_sync(1, 128);
 #pragma unroll
                   for (int q = 0; q < 16; ++q) {
                     const int row = rr * 16 + q;
-                    st_shared_f32(buf + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4,
-                                  __uint_as_float(r[2 * dh + (row >> 5)][row & 31]) * a.scale);
+                    st_shared_f32(buf + q * 512 + rl * 4, __uint_as_float(r[2 * dh + (row >> 5)][row & 31]) * a.scale);
                   }
                   fence_proxy_async_smem();
-                  __syncwarp();
-                  if (lane == 0) {
-                    tma_reduce_add_5d(&tm_dq, buf, dh * 128 + quarter * 32, h, t * QR + rr * 16, c, b);
+                  named_bar_sync(1, 128);
+                  if (rl == 0) {
+                    tma_reduce_add_5d(&tm_dq, buf, dh * 128, h, t * QR + rr * 16, c, b);
                     bulk_commit();
                   }
                 }
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (!ok) break;
     }
-    if (lane == 0) bulk_wait<0>();  // every dQ reduce-add of this warp has completed
+    if (rl == 0) bulk_wait<0>();  // every dQ reduce-add has completed
   }
 
   tc_fence_before();

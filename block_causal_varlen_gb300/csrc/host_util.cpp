@@ -68,9 +68,14 @@ static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_
 
 int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
                              const char* name, int box_cols, int box_rows) {
-  if (box_cols != 16 && box_cols != 32) return fail(BD_ERR_ARG, "%s: reduce box of %d columns", name, box_cols);
-  return make_tmap(map, t, B, C, heads, d, name, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(box_cols),
-                   box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, cuuint32_t(box_rows));
+  if (box_cols != 16 && box_cols != 32 && box_cols != 128)
+    return fail(BD_ERR_ARG, "%s: reduce box of %d columns", name, box_cols);
+  // 16 / 32 columns: 64- / 128-byte swizzled rows; 128 columns: 512-byte rows, unswizzled
+  const CUtensorMapSwizzle swz = box_cols == 32    ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return make_tmap(map, t, B, C, heads, d, name, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(box_cols), swz,
+                   cuuint32_t(box_rows));
 }
 
 int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
