@@ -88,7 +88,8 @@ template <int D, bool DROP>
 __global__ void __launch_bounds__(512, 1)
     bd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, const BwdArgs a) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -575,8 +576,51 @@ __global__ void __launch_bounds__(512, 1)
           }
       }
       if (!ok) break;
-      if (!(ok = mbar_wait(bar(C_ACCDONE), u & 1, abort_flag))) break;
+      // the warpgroup meets at named barriers below when TMA takes the rows out
+      ok = bar_red_and(1, 128, mbar_wait(bar(C_ACCDONE), u & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
+      if (a.tma_dkv) {
+        // dV, then dK (x scale), each leaving TMEM whole first, go out as 128-row x
+        // 32-column boxes through the two staging buffers, stored (or added) by TMA:
+        // one thread's row per lane written 32 bytes at a time by the load/store
+        // unit kept it busy for ~9k cycles a unit, stalling the next unit's loads
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          uint32_t v[D / 32][32];
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + (x ? Cfg::kColDK : Cfg::kColDV) + q * 32, v[q]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) reg_fence(v[q]);
+          tc_fence_before();
+          mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
+          const float mul = x ? a.scale : 1.f;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            const uint32_t buf = sStage + (q & 1) * Cfg::kStageBytes;
+            if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              st_shared_v4(buf + rl * 128 + ((c4 ^ (rl & 7)) << 4),
+                           __float_as_uint(__uint_as_float(v[q][4 * c4]) * mul),
+                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 1]) * mul),
+                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 2]) * mul),
+                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 3]) * mul));
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (rl == 0) {
+              const CUtensorMap* m = x ? &tm_dk : &tm_dv;
+              if (a.accumulate) tma_reduce_add_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
+              else tma_store_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
+              bulk_commit();
+            }
+          }
+        }
+        ++u;
+        continue;
+      }
       // dV, then dK (x scale): each block leaves TMEM whole before it is stored, so
       // that the next unit's first dV / dK MMA can start while the rows go out
 #pragma unroll 1
@@ -649,8 +693,8 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int D, bool DROP>
 static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                          const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdArgs& a, int grid,
-                          cudaStream_t stream) {
+                          const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                          const CUtensorMap& mdv, const BwdArgs& a, int grid, cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -667,7 +711,7 @@ static int32_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
                   fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
-  bd_bwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, mdq, a);
+  bd_bwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mdo, mdq, mdk, mdv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_bwd_kernel launch");
   return BD_OK;
@@ -843,6 +887,13 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
     };
     a.rows32 = (al32(dk) && al32(dv)) ? 1 : 0;
   }
+  // dK / dV by TMA when both tensors admit a tensor map of 128-row x 32-column fp32
+  // boxes (16-byte aligned base and strides); else the threads store the rows
+  CUtensorMap mdk, mdv;
+  a.tma_dkv = 0;
+  if (c.D != 256 && make_tmap_f32_reduce(&mdk, dk, c.B, ck_out, c.Hkv, c.D, "dk", 32, 128) == BD_OK &&
+      make_tmap_f32_reduce(&mdv, dv, c.B, ck_out, c.Hkv, c.D, "dv", 32, 128) == BD_OK)
+    a.tma_dkv = 1;
   float scale;
   const int32_t sb = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &sb, 4);
@@ -861,11 +912,11 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   if (c.D == 256)
     st = launch_bwd256(mq, mk, mv, mdo, mdq, a, a.drop_thresh != 0, grid, s);
   else if (a.drop_thresh != 0)
-    st = c.D == 128 ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, a, grid, s)
-                    : launch_bwd<64, true>(mq, mk, mv, mdo, mdq, a, grid, s);
+    st = c.D == 128 ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, s)
+                    : launch_bwd<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, s);
   else
-    st = c.D == 128 ? launch_bwd<128, false>(mq, mk, mv, mdo, mdq, a, grid, s)
-                    : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, a, grid, s);
+    st = c.D == 128 ? launch_bwd<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, s)
+                    : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, s);
   if (st) return st;
   return ok();
 }
