@@ -59,6 +59,7 @@ struct FwdArgs {
   int64_t z_sb, z_sc, z_sr, z_sh;
   int32_t B, C, H;
   int32_t counter_slot;  // which (claim, done) pair of the plan's forward counter slots
+  int32_t tma_o;         // O has a tensor map: the epilogue stores it by TMA (head dims 64, 128)
 };
 
 template <int D>
@@ -74,7 +75,11 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQSlots * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  // head dims 64 / 128: one 16 KB staging box (128 rows x 64 columns bf16) per slot
+  // through which the epilogue's O rows leave by TMA
+  static constexpr int kStageBytes = 16384;
+  static constexpr int kOffStage = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffBar = kOffStage + (D <= 128 ? 2 * kStageBytes : 0);
   // the 128 rows' document starts of a unit's query tile, two buffers (units in turn)
   static constexpr int kOffDs = kOffBar + 512;
   static constexpr int kSmem = kOffDs + 2 * 512 + 1024;  // + alignment slack
@@ -128,7 +133,8 @@ __device__ __forceinline__ void fwd_unit_take(uint32_t full0, uint32_t empty0, c
 template <int D, bool DROP>
 __global__ void __launch_bounds__(384, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdArgs a) {
   using Cfg = FwdCfg<D>;
   constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -590,7 +596,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         FwdUnit N;
         take(uk + 1, N);
-        if (!(ok = mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag))) break;
+        // the slot's warps meet at named barriers in the epilogue: leave together
+        ok = bar_red_and(1 + s, 128, mbar_wait(bar(B_OFINAL + s), qi & 1, abort_flag));
+        if (!ok) break;
         tc_fence_after();
         const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * (DROP ? a.drop_scale : 1.f);
         if constexpr (D <= 128) {
@@ -604,6 +612,33 @@ __global__ void __launch_bounds__(384, 1)
           for (int q = 0; q < D / 32; ++q) reg_fence(ov[q]);
           tc_fence_before();
           mbar_arrive(bar(B_OEMPTY + s));
+          if (a.tma_o) {
+            // 64 columns at a time through the slot's staging box (row r's 16-byte
+            // chunk c at c ^ (r & 7): the 128-byte swizzle of the map), sent by one
+            // thread with a TMA store (rows past L are clipped); the threads' own row
+            // stores kept the load/store unit busy through the next unit's start
+            const uint32_t sbuf = sbase + Cfg::kOffStage + s * Cfg::kStageBytes;
+#pragma unroll
+            for (int k = 0; k < D / 64; ++k) {
+              if (r == 0) bulk_wait_read<0>();  // the box sent from this buffer before has left it
+              named_bar_sync(1 + s, 128);
+#pragma unroll
+              for (int c8 = 0; c8 < 8; ++c8) {
+                const uint32_t* v = ov[2 * k + (c8 >> 2)] + (c8 & 3) * 8;
+                st_shared_v4(sbuf + r * 128 + ((c8 ^ (r & 7)) << 4),
+                             pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                             pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                             pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                             pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+              }
+              fence_proxy_async_smem();
+              named_bar_sync(1 + s, 128);
+              if (r == 0) {
+                tma_store_5d(&tm_o, sbuf, k * 64, h, U.qtile * 128, c, b);
+                bulk_commit();
+              }
+            }
+          } else {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t pk[16];
@@ -615,6 +650,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
             }
+          }
           }
           if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
         } else {
@@ -641,6 +677,7 @@ __global__ void __launch_bounds__(384, 1)
         ++qi;
         U = N;
       }
+      if (r == 0) bulk_wait<0>();  // the epilogue's TMA stores have completed
     }
   }
 
@@ -660,8 +697,8 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 template <int D, bool DROP>
-static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
-                          int grid, cudaStream_t stream) {
+static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const CUtensorMap& mo, const FwdArgs& a, int grid, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -678,7 +715,7 @@ static int32_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CU
                   fa.numRegs, Cfg::kRegsLaunch);
     attr_done[dev] = true;
   }
-  bd_fwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, a);
+  bd_fwd_kernel<D, DROP><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mq, mk, mv, mo, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bd_fwd_kernel launch");
   return BD_OK;
@@ -733,7 +770,8 @@ extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, c
     if ((st = check_tensor(dq_zero, "dq_zero", 4, B, C, H, false))) return st;
     if (dq_zero->rows != L) return fail(BD_ERR_ARG, "dq_zero rows must equal L = %d", L);
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
+  std::memset(&mo, 0, sizeof(mo));
   if ((st = make_tmap_bf16(&mq, q, B, C, H, D, "q"))) return st;
   if ((st = make_tmap_bf16(&mk, k, B, Ck, Hkv, D, "k"))) return st;
   if ((st = make_tmap_bf16(&mv, v, B, Ck, Hkv, D, "v"))) return st;
@@ -747,6 +785,8 @@ extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, c
   a.z_sb = dq_zero ? dq_zero->stride_b : 0; a.z_sc = dq_zero ? dq_zero->stride_c : 0;
   a.z_sr = dq_zero ? dq_zero->stride_row : 0; a.z_sh = dq_zero ? dq_zero->stride_head : 0;
   a.B = B; a.C = C; a.H = H;
+  // O by TMA when its layout admits a tensor map (16-byte aligned base and strides)
+  a.tma_o = (D <= 128 && make_tmap_bf16(&mo, out, B, C, H, D, "o") == BD_OK) ? 1 : 0;
   // each launch takes the next counter slot: launches sharing the device plan may
   // then overlap on the GPU (up to kFwdCounterSlots at once) without taking each
   // other's work units
@@ -768,13 +808,13 @@ extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, c
   memcpy(&a.drop_scale, &dbits, 4);
   if (D == 256 && a.slots != 1) return fail(BD_ERR_PLAN, "head dim 256 plans use one query head per CTA");
   if (a.drop_thresh != 0)
-    st = D == 256   ? launch_fwd<256, true>(mq, mk, mv, a, grid, s)
-         : D == 128 ? launch_fwd<128, true>(mq, mk, mv, a, grid, s)
-                    : launch_fwd<64, true>(mq, mk, mv, a, grid, s);
+    st = D == 256   ? launch_fwd<256, true>(mq, mk, mv, mo, a, grid, s)
+         : D == 128 ? launch_fwd<128, true>(mq, mk, mv, mo, a, grid, s)
+                    : launch_fwd<64, true>(mq, mk, mv, mo, a, grid, s);
   else
-    st = D == 256   ? launch_fwd<256, false>(mq, mk, mv, a, grid, s)
-         : D == 128 ? launch_fwd<128, false>(mq, mk, mv, a, grid, s)
-                    : launch_fwd<64, false>(mq, mk, mv, a, grid, s);
+    st = D == 256   ? launch_fwd<256, false>(mq, mk, mv, mo, a, grid, s)
+         : D == 128 ? launch_fwd<128, false>(mq, mk, mv, mo, a, grid, s)
+                    : launch_fwd<64, false>(mq, mk, mv, mo, a, grid, s);
   if (st) return st;
   return ok();
 }
