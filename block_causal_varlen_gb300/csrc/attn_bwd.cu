@@ -385,8 +385,12 @@ __global__ void __launch_bounds__(512, 1)
                   if (__shfl_sync(0xffffffffu, ds_mine, ehi + step - 1) <= j) ehi += step;
                 if (__shfl_sync(0xffffffffu, ds_mine, ehi) <= j) ++ehi;
                 const int elo = j - (i0 + ib);
+                // bit e of `seen`: key j sees query e of the chunk (one bit test per element)
+                uint32_t seen = 0u;
+                if (elo < ehi && elo <= 31 && ehi >= 1)
+                  seen = (elo <= 0 ? 0xffffffffu : (0xffffffffu << elo)) & (ehi >= 32 ? 0xffffffffu : ((1u << ehi) - 1u));
 #pragma unroll
-                for (int e = 0; e < 32; ++e) p[e] = (e < elo || e >= ehi) ? 0.f : p[e];
+                for (int e = 0; e < 32; ++e) p[e] = (seen & (1u << e)) ? p[e] : 0.f;
               }
 #pragma unroll
               for (int e = 0; e < 16; ++e) pk[ch][e] = pack_bf16(p[2 * e], p[2 * e + 1]);

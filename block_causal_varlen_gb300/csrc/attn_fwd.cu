@@ -491,9 +491,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[32 * q + e] = -CUDART_INF_F;
               } else if (!__all_sync(0xffffffffu, lo <= 32 * q && hi >= 32 * q + 31)) {
+                // bit e of `seen`: the row sees column 32 q + e (one bit test per element)
+                const int a0 = lo - 32 * q, a1 = hi - 32 * q;
+                uint32_t seen = 0u;
+                if (a1 >= 0 && a0 <= 31 && a1 >= a0)
+                  seen = (a0 <= 0 ? 0xffffffffu : (0xffffffffu << a0)) & (a1 >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - a1)));
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  x[32 * q + e] = (32 * q + e < lo || 32 * q + e > hi) ? -CUDART_INF_F : x[32 * q + e];
+                for (int e = 0; e < 32; ++e) x[32 * q + e] = (seen & (1u << e)) ? x[32 * q + e] : -CUDART_INF_F;
               }
             }
           }
