@@ -584,49 +584,11 @@ __global__ void __launch_bounds__(512, 1)
       ok = bar_red_and(1, 128, mbar_wait(bar(C_ACCDONE), u & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      if (a.tma_dkv) {
-        // dV, then dK (x scale), each leaving TMEM whole first, go out as 128-row x
-        // 32-column boxes through the two staging buffers, stored (or added) by TMA:
-        // one thread's row per lane written 32 bytes at a time by the load/store
-        // unit kept it busy for ~9k cycles a unit, stalling the next unit's loads
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          uint32_t v[D / 32][32];
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) tmem_ld32(tmem + lane_base + (x ? Cfg::kColDK : Cfg::kColDV) + q * 32, v[q]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) reg_fence(v[q]);
-          tc_fence_before();
-          mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
-          const float mul = x ? a.scale : 1.f;
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            const uint32_t buf = sStage + (q & 1) * Cfg::kStageBytes;
-            if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
-            named_bar_sync(1, 128);
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-              st_shared_v4(buf + rl * 128 + ((c4 ^ (rl & 7)) << 4),
-                           __float_as_uint(__uint_as_float(v[q][4 * c4]) * mul),
-                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 1]) * mul),
-                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 2]) * mul),
-                           __float_as_uint(__uint_as_float(v[q][4 * c4 + 3]) * mul));
-            fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (rl == 0) {
-              const CUtensorMap* m = x ? &tm_dk : &tm_dv;
-              if (a.accumulate) tma_reduce_add_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
-              else tma_store_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
-              bulk_commit();
-            }
-          }
-        }
-        ++u;
-        continue;
-      }
-      // dV, then dK (x scale): each block leaves TMEM whole before it is stored, so
-      // that the next unit's first dV / dK MMA can start while the rows go out
+      // dV, then dK (x scale), each leaving TMEM whole first (so that the next
+      // unit's first dV / dK MMA can start), go out as 128-row x 32-column boxes
+      // through the two staging buffers, stored (or added) by TMA: one thread's
+      // row per lane written 32 bytes at a time by the load/store unit kept it busy
+      // for ~9k cycles a unit, stalling the next unit's loads
 #pragma unroll 1
       for (int x = 0; x < 2; ++x) {
         uint32_t v[D / 32][32];
@@ -637,41 +599,26 @@ __global__ void __launch_bounds__(512, 1)
         for (int q = 0; q < D / 32; ++q) reg_fence(v[q]);
         tc_fence_before();
         mbar_arrive(bar(x ? C_DKFREE : C_DVFREE));
-        if (krow_ok) {
-          float* row = x ? dkrow : dvrow;
-          const float mul = x ? a.scale : 1.f;
-          if (a.rows32) {
-            // whole 32-byte sectors per store: the warp's 32 rows lie 4 KB or more apart
+        const float mul = x ? a.scale : 1.f;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q)
+        for (int q = 0; q < D / 32; ++q) {
+          const uint32_t buf = sStage + (q & 1) * Cfg::kStageBytes;
+          if (rl == 0) bulk_wait_read<1>();  // the box sent from this buffer two rounds ago has left it
+          named_bar_sync(1, 128);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float o[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) o[k] = __uint_as_float(v[q][8 * e + k]) * mul;
-                float* p = row + q * 32 + 8 * e;
-                if (a.accumulate) {
-                  float old[8];
-                  ld_global_v8(p, old);
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) o[k] += old[k];
-                }
-                st_global_v8(p, o);
-              }
-          } else {
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float4 o = make_float4(__uint_as_float(v[q][4 * e]) * mul, __uint_as_float(v[q][4 * e + 1]) * mul,
-                                       __uint_as_float(v[q][4 * e + 2]) * mul, __uint_as_float(v[q][4 * e + 3]) * mul);
-                float4* p = reinterpret_cast<float4*>(row + q * 32) + e;
-                if (a.accumulate) {
-                  const float4 old = *p;
-                  o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                }
-                *p = o;
-              }
+          for (int c4 = 0; c4 < 8; ++c4)
+            st_shared_v4(buf + rl * 128 + ((c4 ^ (rl & 7)) << 4),
+                         __float_as_uint(__uint_as_float(v[q][4 * c4]) * mul),
+                         __float_as_uint(__uint_as_float(v[q][4 * c4 + 1]) * mul),
+                         __float_as_uint(__uint_as_float(v[q][4 * c4 + 2]) * mul),
+                         __float_as_uint(__uint_as_float(v[q][4 * c4 + 3]) * mul));
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (rl == 0) {
+            const CUtensorMap* m = x ? &tm_dk : &tm_dv;
+            if (a.accumulate) tma_reduce_add_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
+            else tma_store_5d(m, buf, q * 32, g, W[W_OROW], oc, ob);
+            bulk_commit();
           }
         }
       }
@@ -884,20 +831,15 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   a.work_off = owner ? pv.hdr(H_OFF_BWDO) : pv.hdr(H_OFF_BWD);
   a.ck_out = ck_out;
   a.accumulate = accumulate_dkv ? 1 : 0; a.dk_rows = dk->rows;
-  {
-    auto al32 = [](const bd_tensor* t) {
-      return reinterpret_cast<uintptr_t>(t->ptr) % 32 == 0 && (t->stride_b * 4) % 32 == 0 &&
-             (t->stride_c * 4) % 32 == 0 && (t->stride_row * 4) % 32 == 0 && (t->stride_head * 4) % 32 == 0;
-    };
-    a.rows32 = (al32(dk) && al32(dv)) ? 1 : 0;
-  }
-  // dK / dV by TMA when both tensors admit a tensor map of 128-row x 32-column fp32
-  // boxes (16-byte aligned base and strides); else the threads store the rows
+  // dK / dV leave by TMA in 128-row x 32-column fp32 boxes (the checks above give
+  // the 16-byte aligned base and strides a tensor map needs)
   CUtensorMap mdk, mdv;
-  a.tma_dkv = 0;
-  if (c.D != 256 && make_tmap_f32_reduce(&mdk, dk, c.B, ck_out, c.Hkv, c.D, "dk", 32, 128) == BD_OK &&
-      make_tmap_f32_reduce(&mdv, dv, c.B, ck_out, c.Hkv, c.D, "dv", 32, 128) == BD_OK)
-    a.tma_dkv = 1;
+  std::memset(&mdk, 0, sizeof(mdk));
+  std::memset(&mdv, 0, sizeof(mdv));
+  if (c.D != 256) {
+    if ((st = make_tmap_f32_reduce(&mdk, dk, c.B, ck_out, c.Hkv, c.D, "dk", 32, 128))) return st;
+    if ((st = make_tmap_f32_reduce(&mdv, dv, c.B, ck_out, c.Hkv, c.D, "dv", 32, 128))) return st;
+  }
   float scale;
   const int32_t sb = pv.hdr(H_SCALE_BITS);
   memcpy(&scale, &sb, 4);

@@ -59,7 +59,6 @@ struct FwdArgs {
   int64_t z_sb, z_sc, z_sr, z_sh;
   int32_t B, C, H;
   int32_t counter_slot;  // which (claim, done) pair of the plan's forward counter slots
-  int32_t tma_o;         // O has a tensor map: the epilogue stores it by TMA (head dims 64, 128)
 };
 
 template <int D>
@@ -616,45 +615,30 @@ __global__ void __launch_bounds__(384, 1)
           for (int q = 0; q < D / 32; ++q) reg_fence(ov[q]);
           tc_fence_before();
           mbar_arrive(bar(B_OEMPTY + s));
-          if (a.tma_o) {
-            // 64 columns at a time through the slot's staging box (row r's 16-byte
-            // chunk c at c ^ (r & 7): the 128-byte swizzle of the map), sent by one
-            // thread with a TMA store (rows past L are clipped); the threads' own row
-            // stores kept the load/store unit busy through the next unit's start
-            const uint32_t sbuf = sbase + Cfg::kOffStage + s * Cfg::kStageBytes;
+          // 64 columns at a time through the slot's staging box (row r's 16-byte
+          // chunk c at c ^ (r & 7): the 128-byte swizzle of the map), sent by one
+          // thread with a TMA store (rows past L are clipped); the threads' own row
+          // stores kept the load/store unit busy through the next unit's start
+          const uint32_t sbuf = sbase + Cfg::kOffStage + s * Cfg::kStageBytes;
 #pragma unroll
-            for (int k = 0; k < D / 64; ++k) {
-              if (r == 0) bulk_wait_read<0>();  // the box sent from this buffer before has left it
-              named_bar_sync(1 + s, 128);
+          for (int k = 0; k < D / 64; ++k) {
+            if (r == 0) bulk_wait_read<0>();  // the box sent from this buffer before has left it
+            named_bar_sync(1 + s, 128);
 #pragma unroll
-              for (int c8 = 0; c8 < 8; ++c8) {
-                const uint32_t* v = ov[2 * k + (c8 >> 2)] + (c8 & 3) * 8;
-                st_shared_v4(sbuf + r * 128 + ((c8 ^ (r & 7)) << 4),
-                             pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
-                             pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
-                             pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
-                             pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
-              }
-              fence_proxy_async_smem();
-              named_bar_sync(1 + s, 128);
-              if (r == 0) {
-                tma_store_5d(&tm_o, sbuf, k * 64, h, U.qtile * 128, c, b);
-                bulk_commit();
-              }
+            for (int c8 = 0; c8 < 8; ++c8) {
+              const uint32_t* v = ov[2 * k + (c8 >> 2)] + (c8 & 3) * 8;
+              st_shared_v4(sbuf + r * 128 + ((c8 ^ (r & 7)) << 4),
+                           pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                           pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                           pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                           pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
             }
-          } else {
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16(__uint_as_float(ov[q][2 * e]) * inv, __uint_as_float(ov[q][2 * e + 1]) * inv);
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            fence_proxy_async_smem();
+            named_bar_sync(1 + s, 128);
+            if (r == 0) {
+              tma_store_5d(&tm_o, sbuf, k * 64, h, U.qtile * 128, c, b);
+              bulk_commit();
             }
-          }
           }
           if (row_ok) *lrow_p = l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
         } else {
@@ -789,8 +773,9 @@ extern "C" int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, c
   a.z_sb = dq_zero ? dq_zero->stride_b : 0; a.z_sc = dq_zero ? dq_zero->stride_c : 0;
   a.z_sr = dq_zero ? dq_zero->stride_row : 0; a.z_sh = dq_zero ? dq_zero->stride_head : 0;
   a.B = B; a.C = C; a.H = H;
-  // O by TMA when its layout admits a tensor map (16-byte aligned base and strides)
-  a.tma_o = (D <= 128 && make_tmap_bf16(&mo, out, B, C, H, D, "o") == BD_OK) ? 1 : 0;
+  // O leaves by TMA at head dims 64 / 128 (the checks above give the 16-byte
+  // aligned base and strides a tensor map needs)
+  if (D <= 128 && (st = make_tmap_bf16(&mo, out, B, C, H, D, "o"))) return st;
   // each launch takes the next counter slot: launches sharing the device plan may
   // then overlap on the GPU (up to kFwdCounterSlots at once) without taking each
   // other's work units

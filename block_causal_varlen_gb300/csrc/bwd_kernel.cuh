@@ -25,8 +25,6 @@ struct BwdArgs {
   int32_t L, Lpad, H, G, Ck, n_work, accumulate, dk_rows;
   int32_t work_off;  // plan word offset of the work-unit list the launch walks
   int32_t ck_out;    // chunk extent of the dK / dV output (its buffer index = b * ck_out + c)
-  int32_t rows32;    // every dK / dV row starts 32-byte aligned: rows leave in 32-byte stores
-  int32_t tma_dkv;   // dK / dV have tensor maps: the epilogue stores (or adds) them by TMA
   float scale, scale_log2;
   // attention dropout (used by the DROP instantiations): keep iff Philox word >= thresh
   uint32_t drop_thresh, drop_k0, drop_k1;
