@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "bwd_aux.h"
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(512, 1)
             const int i0 = r0 + t * 128;  // global row of query column 0
             const float* st_lse = reinterpret_cast<const float*>(smem + Cfg::kOffStat + qs * Cfg::kStatBytes);
             const float* st_d = st_lse + 128;
-            // the query rows' document starts come from global memory (the workspace),
+            // the query rows' document starts come from global memory (the plan),
             // read before the waits so that their latency hides behind them: the last
             // row's for the whole-tile test, and lane l's row of each 32-column chunk
             // for masking (shared with the other lanes by shuffles)
@@ -729,8 +730,8 @@ extern "C" int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_de
   BwdCommon c;
   int32_t st = bwd_common(plan_host, plan_dev, workspace, workspace_bytes, &c);
   if (st) return st;
-  if ((st = check_tensor(out, "out", 2, c.B, c.C, c.H, false))) return st;
-  if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, false))) return st;
+  if ((st = check_tensor(out, "out", 2, c.B, c.C, c.H, true))) return st;
+  if ((st = check_tensor(dout, "dout", 2, c.B, c.C, c.H, true))) return st;
   if ((st = check_tensor(dq, "dq", 4, c.B, c.C, c.H, false))) return st;
   if (out->rows != c.L || dout->rows != c.L || dq->rows != c.L)
     return fail(BD_ERR_ARG, "out/dout/dq rows must equal L = %d", c.L);
@@ -738,26 +739,31 @@ extern "C" int32_t bd_attn_bwd_pre_ex(const void* plan_host, const void* plan_de
   char* wsb = static_cast<char*>(workspace);
   BwdPreArgs p;
   p.plan = static_cast<const int32_t*>(plan_dev);
-  p.o = static_cast<const __nv_bfloat16*>(out->ptr);
-  p.o_sb = out->stride_b; p.o_sc = out->stride_c; p.o_sr = out->stride_row; p.o_sh = out->stride_head;
-  p.dout = static_cast<const __nv_bfloat16*>(dout->ptr);
-  p.g_sb = dout->stride_b; p.g_sc = dout->stride_c; p.g_sr = dout->stride_row; p.g_sh = dout->stride_head;
   p.lse = lse->ptr; p.l_sb = lse->stride_b; p.l_sc = lse->stride_c; p.l_sh = lse->stride_head;
   p.lse2 = reinterpret_cast<float*>(wsb + c.ws.lse2);
   p.dstat = reinterpret_cast<float*>(wsb + c.ws.dstat);
-  p.rowds = reinterpret_cast<int32_t*>(wsb + c.ws.rowds);
   p.counters = reinterpret_cast<int32_t*>(wsb + c.ws.counters);
   p.dq = static_cast<float*>(dq->ptr);
   p.q_sb = dq->stride_b; p.q_sc = dq->stride_c; p.q_sr = dq->stride_row; p.q_sh = dq->stride_head;
   p.nitems = c.nitems; p.C = c.C; p.L = c.L; p.Lpad = c.Lpad; p.H = c.H; p.clear_dq = clear_dq ? 1 : 0;
-  p.rowds_off = c.pv.hdr(H_OFF_ROWDS);
+  p.items_off = c.pv.hdr(H_OFF_ITEMS);
   {
-    // up to four 16-byte pieces per thread and block of 256: several rows per block
-    // when a row has few heads
-    const int pieces = c.H * (c.D / 8);
-    p.rows_per_block = pieces <= 256 ? 4 : pieces <= 512 ? 2 : 1;
+    // a group (one shared-memory box of O, one of dO: 8 KB each) holds whole
+    // head-rows: up to 4096 / d heads of a power-of-two number of rows (<= 128,
+    // so that groups tile Lpad)
+    p.heads = std::min(c.H, 4096 / c.D);
+    int rows = 1;
+    while (rows < 128 && 2 * rows * p.heads * c.D * 2 <= 8192) rows *= 2;
+    p.rows = rows;
+    p.head_blocks = (c.H + p.heads - 1) / p.heads;
+    const int64_t ngroups = int64_t(c.nitems) * (c.Lpad / rows) * p.head_blocks;
+    if (ngroups > 0x7fffffff) return fail(BD_ERR_UNSUPPORTED, "too many rows for the statistics kernel");
+    p.ngroups = int32_t(ngroups);
   }
-  if ((st = launch_bwd_pre(p, c.D, static_cast<cudaStream_t>(stream)))) return st;
+  CUtensorMap mo, mdo;
+  if ((st = make_tmap_rows_bf16(&mo, out, c.B, c.C, c.H, c.D, "out", p.heads, p.rows))) return st;
+  if ((st = make_tmap_rows_bf16(&mdo, dout, c.B, c.C, c.H, c.D, "dout", p.heads, p.rows))) return st;
+  if ((st = launch_bwd_pre(mo, mdo, p, c.D, static_cast<cudaStream_t>(stream)))) return st;
   return ok();
 }
 
@@ -818,7 +824,7 @@ int32_t bwd_main_impl(const void* plan_host, const void* plan_dev, const bd_tens
   a.plan = static_cast<const int32_t*>(plan_dev);
   a.lse2 = reinterpret_cast<const float*>(wsb + c.ws.lse2);
   a.dstat = reinterpret_cast<const float*>(wsb + c.ws.dstat);
-  a.rowds = reinterpret_cast<const int32_t*>(wsb + c.ws.rowds);
+  a.rowds = static_cast<const int32_t*>(plan_dev) + pv.hdr(H_OFF_ROWDS);
   a.counters = reinterpret_cast<int32_t*>(wsb + c.ws.counters);
   a.dq = static_cast<float*>(dq->ptr);
   a.q_sb = dq->stride_b; a.q_sc = dq->stride_c; a.q_sr = dq->stride_row; a.q_sh = dq->stride_head;

@@ -1,8 +1,9 @@
 // Small HBM-bound kernels around the backward main loop, plus status readback.
 //
 //   bd_bwd_pre_kernel   D_i = <dO_i, O_i> in fp32 for every (row, head) of every
-//                       chunk, the log2-domain LSE and each row's document
-//                       start, and zeroes the fp32 dQ accumulator rows.
+//                       chunk and the log2-domain LSE; zeroes the main
+//                       kernel's claim counters and (on request) the fp32 dQ
+//                       accumulator rows.
 //   bd_owner_sum_kernel adds needed-only-window dK/dV partials into the rows'
 //                       owners, chunk by chunk in plan order (deterministic);
 //                       the single-GPU form of the index_add / reduce-scatter
@@ -19,112 +20,297 @@
 
 namespace bd {
 
+using namespace dev;
+
 BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdWorkspace w;
   const size_t stat = al(size_t(nitems) * H * Lpad * sizeof(float));
   w.lse2 = 0;
   w.dstat = stat;
-  w.rowds = 2 * stat;
   // the main kernel's work-unit claim counters live in the caller's workspace, so
   // backward launches that share a device plan but not a workspace may overlap
-  w.counters = 2 * stat + al(size_t(nitems) * Lpad * sizeof(int32_t));
+  w.counters = 2 * stat;
   w.total = w.counters + 256;
   return w;
 }
 
-// One block per `rows_per_block` consecutive rows (1, 2 or 4; they divide Lpad, so
-// a block's rows belong to one item): D for every head, the log2-domain LSE, the
-// row's document start, and (unless the caller cleared it already) zeroing of the
-// row's dQ accumulator. Threads take 16-byte pieces of O / dO of all heads of
-// the block's rows, up to four pieces each at a time, so that a thread keeps up
-// to 64 bytes of loads in flight; a head's pieces sit in consecutive lanes and
-// are summed with shuffles. Padding rows (no document) read nothing: their D is
-// 0 and their log2 LSE +inf.
-template <int D>
-__global__ void __launch_bounds__(256) bd_bwd_pre_kernel(BwdPreArgs a) {
-  constexpr int CPH = D / 8;  // 16-byte pieces per head (8, 16 or 32: groups never straddle a warp)
-  const int R = a.rows_per_block;
-  const int64_t grow0 = int64_t(blockIdx.x) * R;  // first row of the block in [nitems, Lpad]
-  const int item = int(grow0 / a.Lpad), l0 = int(grow0 % a.Lpad);
-  const int b = item / a.C, c = item % a.C;
-  const int tid = threadIdx.x;
-  if (blockIdx.x == 0 && tid < 2) a.counters[tid] = 0;  // the main kernel's claim counters
-  const float inf = __int_as_float(0x7f800000);
-  __shared__ int s_ds[4];
-  if (tid < R) {
-    const int l = l0 + tid;
-    int32_t v = 0x7fffffff;
-    if (l < a.L) v = a.plan[a.rowds_off + int64_t(item) * a.Lpad + l];
-    a.rowds[int64_t(item) * a.Lpad + l] = v;
-    s_ds[tid] = v == kRowInvalid ? -1 : v;
+namespace {
+
+constexpr int kPreCtasPerSm = 3;                // CTAs resident per SM (their serial paths overlap)
+constexpr int kPreStages = 4;                   // O + dO boxes in flight per CTA
+constexpr int kPreBoxBytes = 8192;              // one O (or dO) box
+constexpr int kPreStageBytes = 2 * kPreBoxBytes;
+constexpr int kPreConsumers = 256;              // the dot-product warps; the next warp issues the loads
+constexpr int kPreThreads = kPreConsumers + 32;
+constexpr int kPrePieces = kPreBoxBytes / 16 / kPreConsumers;  // 16-byte pieces per consumer thread and box
+constexpr int kPreAhead = 4;                    // groups whose LSE loads are in flight
+constexpr int kPreOffBar = kPreStages * kPreStageBytes;
+constexpr int kPreSmem = kPreOffBar + 2 * kPreStages * 8 + 16 + 1024;  // + alignment slack
+
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+// Read-only global loads kept where they are written (volatile): issued ahead of
+// the waits they are meant to overlap, not moved next to their first use.
+__device__ __forceinline__ float ld_ahead_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ld_ahead_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Walks groups g, g + stride, g + 2 stride, ... as (item, row block, head block),
+// group = (item * row_blocks + row block) * head_blocks + head block, by mixed-radix
+// addition instead of a division per step.
+struct PreIter {
+  int hb, rb, item, dhb, drb, ditem, hbs, nrb;
+  __device__ void init(const BwdPreArgs& a, int g, int stride) {
+    hbs = a.head_blocks;
+    nrb = a.Lpad / a.rows;
+    hb = g % hbs;
+    const int t = g / hbs;
+    rb = t % nrb;
+    item = t / nrb;
+    dhb = stride % hbs;
+    const int ts = stride / hbs;
+    drb = ts % nrb;
+    ditem = ts / nrb;
   }
-  if (a.clear_dq) {
-    const int per_row = a.H * (D / 4);
-    for (int f = tid; f < R * per_row; f += 256) {
-      const int r = f / per_row, k = f % per_row;
-      const int l = l0 + r;
-      if (l >= a.L) continue;
-      const int h = k / (D / 4), col = (k % (D / 4)) * 4;
-      float* p = a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr + int64_t(h) * a.q_sh + col;
-      *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+  __device__ void next() {
+    hb += dhb;
+    int carry = 0;
+    if (hb >= hbs) { hb -= hbs; carry = 1; }
+    rb += drb + carry;
+    carry = 0;
+    if (rb >= nrb) { rb -= nrb; carry = 1; }
+    item += ditem + carry;
+  }
+};
+
+}  // namespace
+
+// D_i = <dO_i, O_i> for every (row, head) of every chunk, the log2-domain LSE
+// (+inf on rows without a document, where D is 0), the main kernel's claim
+// counters zeroed and, unless the caller cleared it already, the fp32 dQ
+// accumulator zeroed. A streaming kernel: kPreCtasPerSm CTAs per SM walk the
+// groups blockIdx.x, blockIdx.x + gridDim.x, ...; a CTA's last warp brings each
+// group's O and dO boxes into a ring of shared-memory stages by TMA (none for
+// groups whose rows are all padding: live rows of an item are [0, L - npad)), and
+// the warps below it take the dot products from shared memory, a (row, head)'s
+// 16-byte pieces in
+// D / 8 consecutive lanes summed with shuffles. The LSE values of a group are
+// loaded kPreAhead - 1 groups ahead so that their latency stays off the stream.
+template <int D>
+__global__ void __launch_bounds__(kPreThreads, kPreCtasPerSm)
+    bd_bwd_pre_kernel(const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_do,
+                      BwdPreArgs a) {
+  constexpr int CPH = D / 8;  // 16-byte pieces per head-row (8, 16 or 32: never straddle a warp)
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  auto full = [&](int s) { return sbase + kPreOffBar + 8u * s; };
+  auto empty = [&](int s) { return sbase + kPreOffBar + 8u * (kPreStages + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPreOffBar + 16 * kPreStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* items = a.plan + a.items_off;
+  const int grid = int(gridDim.x), bid = int(blockIdx.x);
+  // this CTA's groups: bid + k * grid for k < niters
+  const int niters = a.ngroups > bid ? (a.ngroups - bid + grid - 1) / grid : 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPreStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kPreConsumers / 32);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (bid == 0 && threadIdx.x < 2) a.counters[threadIdx.x] = 0;
+  __syncthreads();
+  bool ok = true;
+
+  if (warp == kPreConsumers / 32) {
+    // ---- loads: lane j finds out whether group k + j has a live row, 32 groups at
+    // a time (the next 32 groups' npad loaded while these are issued); lane 0 issues
+    const uint32_t tx = uint32_t(2 * a.rows * a.heads * D * 2);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_o);
+      tma_prefetch_desc(&tm_do);
+    }
+    PreIter li, it0;
+    li.init(a, bid + lane * grid, 32 * grid);  // lane's group of the current batch
+    it0.init(a, bid, grid);                    // lane 0's next group to issue
+    int np = lane < niters ? ld_ahead_s32(items + li.item * kItemWords + I_NPAD) : 0;
+    int issued = 0, s = 0;
+    uint32_t phase = 0;
+    for (int kb = 0; kb < niters && ok; kb += 32) {
+      PreIter ln = li;
+      ln.next();
+      const int np_next = kb + 32 + lane < niters ? ld_ahead_s32(items + ln.item * kItemWords + I_NPAD) : 0;
+      const bool live = kb + lane < niters && li.rb * a.rows < a.L - np;
+      const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
+      if (lane == 0) {
+        const int n = min(32, niters - kb);
+        for (int j = 0; j < n; ++j) {
+          const int k = kb + j;
+          if (k >= kPreStages && !(ok = mbar_wait(empty(s), phase ^ 1u, abort_flag))) break;
+          if ((live_mask >> j) & 1u) {
+            const int b = it0.item / a.C, c = it0.item - b * a.C;
+            const uint32_t st = sbase + uint32_t(s) * kPreStageBytes;
+            mbar_expect_tx(full(s), tx);
+            tma_load_5d(st, &tm_o, full(s), 0, it0.hb * a.heads, it0.rb * a.rows, c, b);
+            tma_load_5d(st + kPreBoxBytes, &tm_do, full(s), 0, it0.hb * a.heads, it0.rb * a.rows, c, b);
+          } else {
+            mbar_arrive(full(s));  // nothing to load: the consumers write the padding values
+          }
+          issued = k + 1;
+          it0.next();
+          if (++s == kPreStages) { s = 0; phase ^= 1u; }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      np = np_next;
+      li = ln;
+    }
+    if (lane == 0 && !ok) {
+      // stop only after the boxes already on their way have landed
+      for (int k = max(0, issued - kPreStages); k < issued; ++k) mbar_wait_drain(full(k % kPreStages), (k / kPreStages) & 1);
+    }
+  } else {
+    // ---- dot products: thread t takes pieces t + i * kPreConsumers of each
+    // group's box, whose (row, head) within the box is the same for every group
+    const int t = threadIdx.x;
+    const int P = a.rows * a.heads * CPH;  // 16-byte pieces per box (<= 512)
+    const float inf = __int_as_float(0x7f800000);
+    int pr[kPrePieces], ph[kPrePieces];
+    bool lead[kPrePieces];
+#pragma unroll
+    for (int i = 0; i < kPrePieces; ++i) {
+      const int p = t + i * kPreConsumers, rh = p / CPH;
+      lead[i] = p < P && p % CPH == 0;
+      pr[i] = rh / a.heads;
+      ph[i] = rh % a.heads;
+    }
+    float lring[kPreAhead][kPrePieces];
+    int nring[kPreAhead];
+    PreIter cur, ahead;
+    cur.init(a, bid, grid);
+    ahead = cur;
+    auto prefetch = [&](int k, float (&lv)[kPrePieces], int& npad) {
+#pragma unroll
+      for (int i = 0; i < kPrePieces; ++i) lv[i] = 0.f;
+      npad = 0;
+      if (k < niters) {
+        npad = ld_ahead_s32(items + ahead.item * kItemWords + I_NPAD);
+        const int b = ahead.item / a.C, c = ahead.item - b * a.C;
+        const float* base = a.lse + b * a.l_sb + c * a.l_sc;
+#pragma unroll
+        for (int i = 0; i < kPrePieces; ++i) {
+          const int h = ahead.hb * a.heads + ph[i], l = ahead.rb * a.rows + pr[i];
+          if (lead[i] && h < a.H && l < a.L) lv[i] = ld_ahead_f32(base + int64_t(h) * a.l_sh + l);
+        }
+      }
+      ahead.next();
+    };
+#pragma unroll
+    for (int j = 0; j < kPreAhead - 1; ++j) prefetch(j, lring[j], nring[j]);
+    int s = 0;
+    uint32_t phase = 0;
+    for (int k0 = 0; k0 < niters && ok; k0 += kPreAhead) {
+#pragma unroll
+      for (int j = 0; j < kPreAhead; ++j) {
+        const int k = k0 + j;
+        if (k >= niters) break;  // the same for every thread of the CTA
+        prefetch(k + kPreAhead - 1, lring[(j + kPreAhead - 1) % kPreAhead], nring[(j + kPreAhead - 1) % kPreAhead]);
+        const int l0 = cur.rb * a.rows, h0 = cur.hb * a.heads, item = cur.item;
+        const int n_live = a.L - nring[j];
+        const bool live = l0 < n_live;  // the same test the load warp made
+        if (!(ok = mbar_wait(full(s), phase, abort_flag))) break;
+        float acc[kPrePieces];
+#pragma unroll
+        for (int i = 0; i < kPrePieces; ++i) acc[i] = 0.f;
+        if (live) {
+          const uint32_t st = sbase + uint32_t(s) * kPreStageBytes;
+#pragma unroll
+          for (int i = 0; i < kPrePieces; ++i) {
+            const int p = t + i * kPreConsumers;
+            if (p < P) {
+              const uint4 ov = ld_shared_u4(st + 16u * p), gv = ld_shared_u4(st + kPreBoxBytes + 16u * p);
+              const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+              const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 x = __bfloat1622float2(o2[e]), y = __bfloat1622float2(g2[e]);
+                acc[i] = fmaf(x.x, y.x, fmaf(x.y, y.y, acc[i]));
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        if (++s == kPreStages) { s = 0; phase ^= 1u; }
+#pragma unroll
+        for (int i = 0; i < kPrePieces; ++i)
+#pragma unroll
+          for (int off = CPH / 2; off > 0; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+#pragma unroll
+        for (int i = 0; i < kPrePieces; ++i) {
+          const int h = h0 + ph[i], l = l0 + pr[i];
+          if (lead[i] && h < a.H) {
+            const bool rl = l < n_live;  // padding rows and rows past L: no attention
+            const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l;
+            a.dstat[sidx] = rl ? acc[i] : 0.f;
+            a.lse2[sidx] = rl ? lring[j][i] * 1.4426950408889634f : inf;
+          }
+        }
+        if (a.clear_dq) {
+          const int b = item / a.C, c = item - b * a.C;
+          for (int f = t; f < 2 * P; f += kPreConsumers) {
+            const int rh = f / (D / 4), l = l0 + rh / a.heads, h = h0 + rh % a.heads, col = (f % (D / 4)) * 4;
+            if (h < a.H && l < a.L)
+              *reinterpret_cast<float4*>(a.dq + b * a.q_sb + c * a.q_sc + int64_t(l) * a.q_sr +
+                                         int64_t(h) * a.q_sh + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        cur.next();
+      }
     }
   }
   __syncthreads();
-  const int npieces = a.H * CPH;  // per row
-  const int total = R * npieces;
-  for (int f0 = 0; f0 < total; f0 += 1024) {
-    uint4 ov[4], gv[4];
-    float lv[4];
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int f = f0 + rr * 256 + tid;
-      ov[rr] = gv[rr] = make_uint4(0u, 0u, 0u, 0u);
-      lv[rr] = 0.f;
-      if (f < total) {
-        const int r = f / npieces, k = f % npieces;
-        if (s_ds[r] >= 0) {
-          const int l = l0 + r, h = k / CPH, col = (k % CPH) * 8;
-          ov[rr] = *reinterpret_cast<const uint4*>(a.o + b * a.o_sb + c * a.o_sc + int64_t(l) * a.o_sr +
-                                                   int64_t(h) * a.o_sh + col);
-          gv[rr] = *reinterpret_cast<const uint4*>(a.dout + b * a.g_sb + c * a.g_sc + int64_t(l) * a.g_sr +
-                                                   int64_t(h) * a.g_sh + col);
-          if (k % CPH == 0) lv[rr] = a.lse[b * a.l_sb + c * a.l_sc + int64_t(h) * a.l_sh + l];
-        }
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      if (f0 + rr * 256 >= total) break;  // the same for the whole block: every lane shuffles
-      const int f = f0 + rr * 256 + tid;
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[rr]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[rr]);
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
-        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-      }
-#pragma unroll
-      for (int off = CPH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (f < total && (f % CPH) == 0) {
-        const int r = f / npieces, h = (f % npieces) / CPH;
-        const bool live = s_ds[r] >= 0;  // padding rows and rows past L: no attention
-        const int64_t sidx = (int64_t(item) * a.H + h) * a.Lpad + l0 + r;
-        a.dstat[sidx] = live ? acc : 0.f;
-        a.lse2[sidx] = live ? lv[rr] * 1.4426950408889634f : inf;
-      }
-    }
+  if (threadIdx.x == 0 && *abort_flag) {
+    atomicExch(const_cast<int32_t*>(a.plan) + H_STATUS, DEV_TIMEOUT);
+    atomicExch(const_cast<int32_t*>(a.plan) + H_STATUS_DETAIL, 4);
   }
 }
 
-int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s) {
-  const int64_t blocks = int64_t(a.nitems) * a.Lpad / a.rows_per_block;
-  if (blocks == 0) return BD_OK;
-  if (blocks > 0x7fffffff) return fail(BD_ERR_UNSUPPORTED, "too many rows for the statistics kernel");
-  if (D == 256) bd_bwd_pre_kernel<256><<<unsigned(blocks), 256, 0, s>>>(a);
-  else if (D == 128) bd_bwd_pre_kernel<128><<<unsigned(blocks), 256, 0, s>>>(a);
-  else bd_bwd_pre_kernel<64><<<unsigned(blocks), 256, 0, s>>>(a);
+int32_t launch_bwd_pre(const CUtensorMap& mo, const CUtensorMap& mdo, const BwdPreArgs& a, int D, cudaStream_t s) {
+  if (a.ngroups == 0) return BD_OK;
+  int nsm = 0;
+  int32_t st = sm_count(&nsm);
+  if (st) return st;
+  const int grid = a.ngroups < kPreCtasPerSm * nsm ? a.ngroups : kPreCtasPerSm * nsm;
+  static bool attr_done[64][3] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int di = D == 256 ? 2 : D == 128 ? 1 : 0;
+  if (dev < 64 && !attr_done[dev][di]) {
+    cudaError_t e = D == 256   ? cudaFuncSetAttribute(bd_bwd_pre_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreSmem)
+                    : D == 128 ? cudaFuncSetAttribute(bd_bwd_pre_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreSmem)
+                               : cudaFuncSetAttribute(bd_bwd_pre_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd pre)");
+    attr_done[dev][di] = true;
+  }
+  if (D == 256) bd_bwd_pre_kernel<256><<<grid, kPreThreads, kPreSmem, s>>>(mo, mdo, a);
+  else if (D == 128) bd_bwd_pre_kernel<128><<<grid, kPreThreads, kPreSmem, s>>>(mo, mdo, a);
+  else bd_bwd_pre_kernel<64><<<grid, kPreThreads, kPreSmem, s>>>(mo, mdo, a);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? BD_OK : cuda_fail(e, "bd_bwd_pre_kernel launch");
 }

@@ -1,5 +1,6 @@
 // Argument blocks of the backward's auxiliary kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -8,26 +9,24 @@ namespace bd {
 
 struct BwdPreArgs {
   const int32_t* plan;
-  const __nv_bfloat16* o;
-  int64_t o_sb, o_sc, o_sr, o_sh;
-  const __nv_bfloat16* dout;
-  int64_t g_sb, g_sc, g_sr, g_sh;
   const float* lse;
   int64_t l_sb, l_sc, l_sh;
   float* lse2;     // workspace [nitems, H, Lpad]: LSE * log2(e), +inf on invalid rows
   float* dstat;    // workspace [nitems, H, Lpad]: D = <dO, O>
-  int32_t* rowds;  // workspace [nitems, Lpad]: global start row of the row's document, INT_MAX if invalid
   int32_t* counters;  // workspace: the main kernel's (claim, done) work-unit counters, zeroed here
   float* dq;       // zeroed when clear_dq is set
   int64_t q_sb, q_sc, q_sr, q_sh;
   int32_t nitems, C, L, Lpad, H, clear_dq;
-  int32_t rowds_off;       // word offset of the plan's per-row document starts ([nitems, Lpad])
-  int32_t rows_per_block;  // 1, 2 or 4 rows per block (set by launch_bwd_pre's caller)
+  int32_t items_off;  // word offset of the plan's chunk items
+  // a group is `rows` consecutive rows x `heads` heads of one item: the O / dO box
+  // one stage of the statistics kernel holds; groups are numbered
+  // ((item * (Lpad / rows) + row block) * head_blocks + head block)
+  int32_t rows, heads, head_blocks, ngroups;
 };
 
 // Workspace layout of the backward (offsets in bytes, 256-byte aligned).
 struct BwdWorkspace {
-  size_t lse2, dstat, rowds, counters, total;
+  size_t lse2, dstat, counters, total;
 };
 BwdWorkspace bwd_workspace_layout(int nitems, int H, int Lpad);
 
@@ -43,6 +42,7 @@ struct OwnerSumArgs {
   int32_t accumulate;  // 1: add the sum into dk / dv; 0: overwrite them with it
 };
 
-int32_t launch_bwd_pre(const BwdPreArgs& a, int D, cudaStream_t s);
+// Launches the statistics kernel over maps of O and dO with the args' row box.
+int32_t launch_bwd_pre(const CUtensorMap& mo, const CUtensorMap& mdo, const BwdPreArgs& a, int D, cudaStream_t s);
 
 }  // namespace bd

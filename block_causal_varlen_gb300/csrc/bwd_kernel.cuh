@@ -14,7 +14,7 @@ struct BwdArgs {
   const int32_t* plan;
   const float* lse2;
   const float* dstat;
-  const int32_t* rowds;
+  const int32_t* rowds;  // the plan's per-row document starts, [nitems][Lpad]
   int32_t* counters;  // (claim, done) work-unit counters in the workspace
   float* dq;
   int64_t q_sb, q_sc, q_sr, q_sh;

@@ -46,7 +46,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
                          const char* name, int esize, CUtensorMapDataType dtype, cuuint32_t box0,
-                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, cuuint32_t box_rows = 128) {
+                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, cuuint32_t box_rows = 128,
+                         cuuint32_t box_heads = 1) {
   auto fn = encode_fn();
   if (!fn) return fail(BD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
   auto fix = [esize](int64_t stride_elems, int64_t ext, int64_t fallback) {
@@ -58,7 +59,7 @@ static int32_t make_tmap(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_
   const int64_t sb = fix(t->stride_b, B, sc * C);
   cuuint64_t dims[5] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(t->rows), cuuint64_t(C), cuuint64_t(B)};
   cuuint64_t strides[4] = {cuuint64_t(sh), cuuint64_t(sr), cuuint64_t(sc), cuuint64_t(sb)};
-  cuuint32_t box[5] = {box0, 1, box_rows, 1, 1};
+  cuuint32_t box[5] = {box0, box_heads, box_rows, 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(map, dtype, 5, t->ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -82,6 +83,15 @@ int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t 
                        const char* name, int box_rows) {
   return make_tmap(map, t, B, C, heads, d, name, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, CU_TENSOR_MAP_SWIZZLE_128B,
                    cuuint32_t(box_rows));
+}
+
+int32_t make_tmap_rows_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                            const char* name, int box_heads, int box_rows) {
+  if (d > 256 || box_heads < 1 || box_heads > 256 || box_rows < 1 || box_rows > 256)
+    return fail(BD_ERR_ARG, "%s: row box of %lld columns x %d heads x %d rows", name, (long long)d, box_heads,
+                box_rows);
+  return make_tmap(map, t, B, C, heads, d, name, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(d),
+                   CU_TENSOR_MAP_SWIZZLE_NONE, cuuint32_t(box_rows), cuuint32_t(box_heads));
 }
 
 int32_t sm_count(int* out) {

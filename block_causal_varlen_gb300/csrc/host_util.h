@@ -26,6 +26,12 @@ int32_t make_tmap_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t 
 int32_t make_tmap_f32_reduce(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
                              const char* name, int box_cols = 16, int box_rows = 128);
 
+// Encodes a 5-D tiled TMA map over bf16 [B, C, rows, heads, d] whose box is whole
+// rows of d columns for box_heads heads x box_rows rows, unswizzled (row-major in
+// shared memory: head-row h of row r at (r * box_heads + h) * d elements).
+int32_t make_tmap_rows_bf16(CUtensorMap* map, const bd_tensor* t, int64_t B, int64_t C, int64_t heads, int64_t d,
+                            const char* name, int box_heads, int box_rows);
+
 // Number of SMs of the current device (cached per device).
 int32_t sm_count(int* out);
 

@@ -257,9 +257,9 @@ BD_API int32_t bd_attn_fwd_ex(const void* plan_host, const void* plan_dev, const
                        bd_tensor* out, bd_rowstat* lse, bd_tensor* dq_zero, void* stream);
 
 /* Workspace bytes bd_attn_bwd needs for this plan: per row and head D = <dO, O>
- * and the LSE in log2 units, each row's document start, and the main kernel's
- * work-unit counters (zeroed by bd_attn_bwd_pre). Calls that overlap on the GPU
- * need workspaces of their own. */
+ * and the LSE in log2 units, and the main kernel's work-unit counters (zeroed
+ * by bd_attn_bwd_pre). Calls that overlap on the GPU need workspaces of their
+ * own. */
 BD_API int32_t bd_attn_bwd_workspace(const void* plan_host, size_t* bytes);
 
 /* bd_attn_bwd -- backward of every chunk item in the plan for the loss
@@ -308,8 +308,9 @@ BD_API int32_t bd_attn_bwd_ex(const void* plan_host, const void* plan_dev, const
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* bd_attn_bwd_pre -- the first step of bd_attn_bwd on its own: per row and
- * head D = <dout, out> (fp32), the LSE in log2 units and each row's document
- * start, written into `workspace`; zeroes dq. */
+ * head D = <dout, out> (fp32) and the LSE in log2 units, written into
+ * `workspace`; zeroes dq. out and dout are read by TMA: their base and strides
+ * must be 16-byte aligned (else BD_ERR_ALIGN before any launch). */
 BD_API int32_t bd_attn_bwd_pre(const void* plan_host, const void* plan_dev, const bd_tensor* out,
                         const bd_tensor* dout, const bd_rowstat* lse, bd_tensor* dq, void* workspace,
                         size_t workspace_bytes, void* stream);
