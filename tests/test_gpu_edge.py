@@ -84,3 +84,42 @@ def test_edge_layout_fwd_bwd(name, mode, d):
         sv = cu[-1]
         assert not dq.view(wl.S, wl.H, wl.d)[sv:].abs().sum().item()
         assert not dk[0, 0, sv:].abs().sum().item() and not dv[0, 0, sv:].abs().sum().item()
+
+
+# Head counts that do not fill the statistics kernel's head blocks (at most
+# 4096 / d heads of whole rows per 8 KB box: 40 heads at d 128 and 24 at d 256 leave
+# the second block partly past H), odd small counts (3 heads at d 64: 16-row boxes
+# of 384 pieces), on chunks of 201 rows (a box straddles L) whose last 22 rows are
+# padding.
+HEAD_SHAPES = [(40, 8, 128), (3, 1, 64), (24, 8, 256), (6, 2, 128)]
+
+
+@pytest.mark.parametrize("H,Hkv,d", HEAD_SHAPES)
+def test_head_counts_fwd_bwd(H, Hkv, d):
+    cu = [0, 37, 150, 380]
+    wl = dataclasses.replace(workloads.config(1), name=f"heads_{H}_{Hkv}_{d}", S=402, cp=2, cu=[cu], H=H, Hkv=Hkv,
+                             d=d)
+    q, k, v, do = workloads.tensors(wl)
+    plan, out, lse, (qd, kd, vd) = gu.run_fwd(wl, q, k, v, bd.BD_KV_GATHER)
+    dod = gu.as_chunks(do.cuda(), wl.cp)
+    dq = torch.full(qd.shape, float("nan"), dtype=torch.float32, device="cuda")
+    dk = torch.zeros(kd.shape, dtype=torch.float32, device="cuda")
+    dv = torch.zeros_like(dk)
+    ws = torch.empty(bd.bd_attn_bwd_workspace(plan), dtype=torch.uint8, device="cuda")
+    bd.bd_attn_bwd(plan, qd, kd, vd, out, dod, lse, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    bd.bd_check_status(plan)
+    out, lse, dq, dk, dv = (t.cpu() for t in (out, lse, dq, dk, dv))
+    dq_ref, dk_ref, dv_ref, o_ref, l_ref = oracle.attention_bwd(q[0], k[0], v[0], do[0], cu)
+    for r in range(wl.cp):
+        rows = slice(r * wl.L, (r + 1) * wl.L)
+        gu.o_check(out[0, r].float(), o_ref[rows])
+        gu.lse_check(lse[0, r], l_ref[:, rows])
+    assert torch.isfinite(dq).all()
+    assert gu.max_rel(dq.reshape(wl.S, H, d), dq_ref) <= gu.GRAD_REL
+    assert gu.max_rel(dk[0, 0], dk_ref) <= gu.GRAD_REL
+    assert gu.max_rel(dv[0, 0], dv_ref) <= gu.GRAD_REL
+    assert gu.doc_rel(dq.reshape(wl.S, H, d), dq_ref, cu) <= gu.GRAD_REL
+    assert gu.doc_rel(dk[0, 0], dk_ref, cu) <= gu.GRAD_REL
+    # padding rows: no gradient
+    assert torch.count_nonzero(dq.reshape(wl.S, H, d)[cu[-1]:]) == 0
