@@ -44,7 +44,7 @@ constexpr int kPreStageBytes = 2 * kPreBoxBytes;
 constexpr int kPreConsumers = 256;              // the dot-product warps; the next warp issues the loads
 constexpr int kPreThreads = kPreConsumers + 32;
 constexpr int kPrePieces = kPreBoxBytes / 16 / kPreConsumers;  // 16-byte pieces per consumer thread and box
-constexpr int kPreAhead = 4;                    // groups whose LSE loads are in flight
+constexpr int kPreAhead = 4;                    // LSE ring: loads issued kPreAhead - 1 groups ahead
 constexpr int kPreOffBar = kPreStages * kPreStageBytes;
 constexpr int kPreSmem = kPreOffBar + 2 * kPreStages * 8 + 16 + 1024;  // + alignment slack
 
