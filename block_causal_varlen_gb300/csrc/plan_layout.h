@@ -27,7 +27,8 @@ enum : int {
   H_FWD_SLOTS = 38,     // kFwdCounterSlots (claim, done) pairs of forward work-unit
                         // counters, one pair per launch in flight (0 between launches)
   H_STATUS = 56,        // written by kernels: 0 = ok, else a device failure code
-  H_STATUS_DETAIL = 57, // where it happened (role/barrier id)
+  H_STATUS_DETAIL = 57, // where it happened: 1 forward, 2 backward main (either head dim),
+                        // 4 backward statistics, 99 the bounded-wait self test
   kHdrWords = 64
 };
 
