@@ -270,6 +270,10 @@ int32_t build(const bd_plan_desc* d, Built* out) {
       }
     }
   }
+  // CTAs per GPU the list orders assume (a GB300 runs one CTA per SM on its 152 SMs)
+  // and the band width divisor of the length-band ordering (see the backward lists)
+  constexpr int64_t kOrderCtas = 152, kBandDiv = 8;
+  constexpr int64_t kShortFwdUnit = 5;  // mean key tiles per forward unit at or below which bands apply
   // ---- forward work: (item, query tile, head slot group), longest first -------------
   struct FW { int32_t w[kFwdWords]; };
   std::vector<FW> fw;
@@ -299,7 +303,25 @@ int32_t build(const bd_plan_desc* d, Built* out) {
         }
     }
   }
-  std::stable_sort(fw.begin(), fw.end(), [](const FW& x, const FW& y) { return x.w[F_NT] > y.w[F_NT]; });
+  // Longest first. When the units are short (at most 5 key tiles on average per
+  // unit that has any), a K/V tile's readers are a few neighbouring query tiles, and
+  // the forward streams K/V from DRAM near the bandwidth limit unless those run at
+  // the same time: such lists run longest first only down to bands of similar
+  // length (the backward lists' ordering, below) and in position order within a
+  // band, so that neighbouring query tiles share their key tiles through L2. On
+  // layouts of longer units that order measured slower than plain longest first.
+  {
+    int64_t total = 0, live = 0;
+    for (const FW& x : fw) {
+      total += x.w[F_NT];
+      live += x.w[F_NT] > 0;
+    }
+    const int64_t band = live > 0 && total <= kShortFwdUnit * live
+                             ? std::max<int64_t>(1, total / (kOrderCtas * kBandDiv))
+                             : 1;
+    std::stable_sort(fw.begin(), fw.end(),
+                     [band](const FW& x, const FW& y) { return x.w[F_NT] / band > y.w[F_NT] / band; });
+  }
   for (const FW& f : fw) P.fwd.insert(P.fwd.end(), f.w, f.w + kFwdWords);
 
   // ---- backward work: (K/V buffer, key tile, K/V head), most query tiles first -------
@@ -332,7 +354,6 @@ int32_t build(const bd_plan_desc* d, Built* out) {
   // steps over kOrderCtas CTAs (a GB300 runs one CTA per SM on its 152 SMs); the
   // finishing spread this adds is at most one band. Layouts of short documents,
   // whose units are all shorter than a band, run in position order.
-  constexpr int64_t kOrderCtas = 152, kBandDiv = 8;
   auto lpt_order = [&](std::vector<BW>& v) {
     int64_t total = 0;
     for (const BW& x : v) total += x.w[W_NQ];
