@@ -362,3 +362,36 @@ def test_visited_tiles_match_brute_force(i):
                         tiles.update(range(start[r] // 128, r // 128 + 1))
                     want += len(tiles)
         assert plan.fwd_tiles() * plan.slots() == want * wl.H, (i, mode)
+
+
+_H_OFF_FWD, _H_NFWD, _H_SLOTS, _FWD_WORDS = 17, 18, 24, 8
+
+
+@pytestmark_lib
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("i", [1, 2, 3, 4, 5])
+def test_plan_forward_list_order(i, d):
+    """The forward work list holds every (item, query tile, head pair) once and runs
+    longest unit first; lists whose units visit at most 5 key tiles on average (per
+    unit that visits any) run in length bands instead (band = the key-tile total
+    over 152 x 8, longest band first) with the units of a band in position order
+    (item, query tile, first head). Ties always keep position order."""
+    wl = workloads.config(i)
+    plan = lib.Plan(wl.cu, wl.S, wl.cp, wl.H, wl.Hkv, d, kv_mode=lib.BD_KV_WINDOW)
+    h = plan.host
+    fw = h[h[_H_OFF_FWD]:h[_H_OFF_FWD] + h[_H_NFWD] * _FWD_WORDS].reshape(-1, _FWD_WORDS)
+    slots = int(h[_H_SLOTS])
+    keys = [tuple(int(x) for x in u[:3]) for u in fw]
+    want = {(it, t, h0) for it in range(wl.B * wl.cp) for t in range(-(-wl.L // 128))
+            for h0 in range(0, wl.H, slots)}
+    assert len(keys) == len(set(keys)) and set(keys) == want
+    nt = fw[:, 4].astype(np.int64)
+    live = int((nt > 0).sum())
+    band = max(1, int(nt.sum()) // (152 * 8)) if live and nt.sum() <= 5 * live else 1
+    b = nt // band
+    assert (np.diff(b) <= 0).all(), "bands must not grow along the list"
+    for j in range(1, len(keys)):
+        if b[j] == b[j - 1]:
+            assert keys[j] > keys[j - 1], f"unit {j} breaks position order inside its band"
+    # the short-document layout is the one that takes bands here
+    assert (band > 1) == (i == 5)
